@@ -1,0 +1,232 @@
+"""Pins for the oracle's encoder: rotation, centroid coding, bit packing, norm
+correction, value quantisation and the page layout."""
+import numpy as np
+import pytest
+
+D = 128
+
+
+def _H():
+    i = np.arange(D)
+    pc = np.vectorize(lambda x: bin(x).count("1"))(i[:, None] & i[None, :])
+    return np.where(pc % 2 == 0, 1.0, -1.0)
+
+
+# ----------------------------------------------------------------- rotation
+
+def test_wht_is_sylvester_hadamard(oracle_lib):
+    O = oracle_lib
+    H = _H()
+    M32 = np.stack([O.wht_f32(np.eye(D)[j]) for j in range(D)], axis=1)
+    M64 = np.stack([O.wht_f64(np.eye(D)[j]) for j in range(D)], axis=1)
+    assert np.array_equal(M32, H)
+    assert np.array_equal(M64, H)
+    assert np.array_equal(H @ H.T, D * np.eye(D))
+
+
+def test_wht_twice_scales_by_D(oracle_lib):
+    rng = np.random.default_rng(1)
+    x = rng.integers(-50, 50, D).astype(np.float64)
+    assert np.array_equal(oracle_lib.wht_f64(oracle_lib.wht_f64(x)), D * x)
+    assert np.array_equal(oracle_lib.wht_f32(oracle_lib.wht_f32(x)), (D * x).astype(np.float32))
+
+
+def test_wht_matches_matrix_product(oracle_lib):
+    rng = np.random.default_rng(2)
+    H = _H()
+    for _ in range(5):
+        x = rng.standard_normal(D)
+        assert np.allclose(oracle_lib.wht_f64(x), H @ x, atol=1e-12, rtol=0)
+        x16 = x.astype(np.float16).astype(np.float64)
+        y = oracle_lib.wht_f32(x16)
+        assert np.allclose(y, H @ x16, atol=1e-5, rtol=0)
+
+
+def test_tree_sum_close_to_exact(oracle_lib):
+    rng = np.random.default_rng(3)
+    for _ in range(20):
+        a = (rng.standard_normal(D) ** 2).astype(np.float32)
+        exact = float(np.sum(a.astype(np.float64)))
+        assert abs(oracle_lib.tree_sum(a) - exact) <= 8 * np.spacing(np.float32(exact))
+    ints = rng.integers(0, 1000, D).astype(np.float32)
+    assert oracle_lib.tree_sum(ints) == float(ints.sum())
+
+
+# ---------------------------------------------------------- centroid coding
+
+def test_quant_index_cells(oracle_lib):
+    O = oracle_lib
+    cb16 = O.codebook16()
+    cb = cb16.view(np.float16).astype(np.float32)
+    for m in range(8):
+        assert O.quant_index(float(cb[m]), cb16) == m
+    for m in range(7):
+        bm = np.float32((np.float64(cb[m]) + np.float64(cb[m + 1])) / 2)
+        assert O.quant_index(float(bm), cb16) == m            # a tie goes low
+        up = np.nextafter(bm, np.float32(np.inf))
+        assert O.quant_index(float(up), cb16) == m + 1
+    assert O.quant_index(0.0, cb16) == 3
+    assert O.quant_index(-1.0, cb16) == 0 and O.quant_index(1.0, cb16) == 7
+
+
+def test_pack3_bit_definition(oracle_lib):
+    rng = np.random.default_rng(4)
+    pats = [np.zeros(D, np.uint8), np.full(D, 7, np.uint8), np.arange(D, dtype=np.uint8) % 8,
+            (7 - np.arange(D) % 8).astype(np.uint8)] + [rng.integers(0, 8, D).astype(np.uint8)
+                                                         for _ in range(20)]
+    for idx in pats:
+        packed = oracle_lib.pack3(idx)
+        stream = 0
+        for j, c in enumerate(idx):
+            stream |= int(c) << (3 * j)
+        assert bytes(packed) == stream.to_bytes(48, "little")
+        assert np.array_equal(oracle_lib.unpack3(packed), idx)
+
+
+def _one_token_page(O, preset, k, v):
+    cache = np.zeros((1, 1, O.page_bytes(preset)), np.uint8)
+    O.store(preset, cache, k.reshape(1, 1, D), v.reshape(1, 1, D), np.array([0], np.int32))
+    return cache[0, 0]
+
+
+def test_centroid_vectors_round_trip(oracle_lib):
+    """A key built as H c (c a vector of centroids) is coded back to c."""
+    O = oracle_lib
+    rng = np.random.default_rng(5)
+    cb16 = O.codebook16()
+    cb = cb16.view(np.float16).astype(np.float64)
+    bnd = 0.5 * (cb[:-1] + cb[1:])
+    for _ in range(30):
+        y = rng.standard_normal(D) / np.sqrt(D)
+        idx = np.searchsorted(bnd, y, side="left").astype(np.uint8)
+        c = cb[idx]
+        k = (2.0 * (_H() @ c)).astype(np.float16)
+        codes, nc = O.encode_key3(k)
+        assert np.array_equal(O.unpack3(codes), idx)
+
+
+def test_norm_correction_preserves_norm(oracle_lib):
+    O = oracle_lib
+    rng = np.random.default_rng(6)
+    for scale in (0.01, 1.0, 30.0):
+        for _ in range(20):
+            k = (rng.standard_normal(D) * scale).astype(np.float16)
+            page = _one_token_page(O, 1, k, np.zeros(D, np.float16))
+            kh = O.decode_key(1, page, 0)
+            nk = np.linalg.norm(k.astype(np.float64))
+            assert abs(np.linalg.norm(kh) / nk - 1.0) <= 2.0 ** -10
+
+
+def test_key3_distortion_matches_lloyd_max(oracle_lib):
+    """Mean relative squared error of norm-corrected 3-bit keys: with
+    distortion d = 0.03454 of the unit-Gaussian Lloyd-Max quantiser, the
+    rescaled reconstruction has cos = sqrt(1 - d), so the relative error is
+    2 - 2 sqrt(1 - d) = 0.0348 (high-dimension limit)."""
+    O = oracle_lib
+    rng = np.random.default_rng(7)
+    errs = []
+    for _ in range(1500):
+        k = rng.standard_normal(D).astype(np.float16)
+        page = _one_token_page(O, 1, k, np.zeros(D, np.float16))
+        kh = O.decode_key(1, page, 0)
+        kk = k.astype(np.float64)
+        errs.append(np.sum((kk - kh) ** 2) / np.sum(kk ** 2))
+    expect = 2 - 2 * np.sqrt(1 - 0.03454)
+    assert abs(np.mean(errs) / expect - 1) < 0.04
+
+
+def test_zero_key(oracle_lib):
+    codes, nc = oracle_lib.encode_key3(np.zeros(D, np.float16))
+    assert nc == 0
+    assert np.array_equal(oracle_lib.unpack3(codes), np.full(D, 3, np.uint8))
+
+
+def test_key8_is_per_coordinate_e4m3(oracle_lib):
+    O = oracle_lib
+    rng = np.random.default_rng(8)
+    k = (rng.standard_normal(D) * 20).astype(np.float16)
+    out = O.encode_key8(k)
+    ref = np.array([O.e4m3_from_half(int(b)) for b in k.view(np.uint16)], np.uint8)
+    assert np.array_equal(out, ref)
+
+
+# ------------------------------------------------------------------ values
+
+def _decode_v(packed, s, z):
+    sf = np.float64(np.array([s], np.uint16).view(np.float16)[0])
+    zf = np.float64(np.array([z], np.uint16).view(np.float16)[0])
+    codes = np.empty(D, np.int64)
+    codes[0::2] = packed & 15
+    codes[1::2] = packed >> 4
+    return codes, codes * sf + zf, sf, zf
+
+
+def test_value_error_bound(oracle_lib):
+    rng = np.random.default_rng(9)
+    for scale in (1e-3, 1.0, 100.0):
+        for _ in range(50):
+            v = (rng.standard_normal(D) * scale).astype(np.float16)
+            packed, s, z = oracle_lib.encode_value4(v)
+            codes, vh, sf, zf = _decode_v(packed, s, z)
+            vv = v.astype(np.float64)
+            assert codes.min() >= 0 and codes.max() <= 15
+            assert sf * 15 >= (vv.max() - vv.min()) * (1 - 1e-7)
+            assert np.all(np.abs(vv - vh) <= sf / 2 * (1 + 1e-6) + 1e-12)
+            assert zf == vv.min()
+
+
+def test_value_constant_and_signed_zero(oracle_lib):
+    for c in (0.0, -0.0, 1.5, -3.25):
+        v = np.full(D, c, np.float16)
+        packed, s, z = oracle_lib.encode_value4(v)
+        codes, vh, sf, zf = _decode_v(packed, s, z)
+        assert s == 0 and np.all(codes == 0)
+        assert np.array_equal(vh, v.astype(np.float64))
+        if c == 0.0:
+            assert z == 0  # -0 is stored as +0
+
+
+def test_value_grid_is_lossless(oracle_lib):
+    rng = np.random.default_rng(10)
+    for s, z in ((0.125, -1.0), (0.0625, 0.5), (0.25, -2.0)):
+        codes = rng.integers(0, 16, D)
+        codes[:2] = (0, 15)
+        v = (z + codes * s).astype(np.float16)
+        packed, sh, zh = oracle_lib.encode_value4(v)
+        got, vh, sf, zf = _decode_v(packed, sh, zh)
+        assert np.array_equal(got, codes) and sf == s and zf == z
+
+
+# -------------------------------------------------------------- page layout
+
+@pytest.mark.parametrize("preset,offs", [(0, dict(k=0, v=2048, s=3072, z=3104, page=3136)),
+                                          (1, dict(k=0, nc=768, v=800, s=1824, z=1856, page=1920))])
+def test_page_layout_and_skips(oracle_lib, preset, offs):
+    O = oracle_lib
+    rng = np.random.default_rng(11)
+    nb, hk = 3, 2
+    assert O.page_bytes(preset) == offs["page"]
+    cache = np.zeros((nb, hk, offs["page"]), np.uint8)
+    T = 5
+    k = rng.standard_normal((T, hk, D)).astype(np.float16)
+    v = rng.standard_normal((T, hk, D)).astype(np.float16)
+    slots = np.array([17, -1, 3, nb * 16, 40], np.int32)
+    O.store(preset, cache, k, v, slots)
+    expect = np.zeros_like(cache)
+    for t, slot in enumerate(slots):
+        if slot < 0 or slot >= nb * 16:
+            continue
+        blk, off = divmod(int(slot), 16)
+        for h in range(hk):
+            pg = expect[blk, h]
+            vp, s, z = O.encode_value4(v[t, h])
+            if preset == 0:
+                pg[off * 128:(off + 1) * 128] = O.encode_key8(k[t, h])
+            else:
+                codes, nc = O.encode_key3(k[t, h])
+                pg[off * 48:(off + 1) * 48] = codes
+                pg[offs["nc"] + 2 * off: offs["nc"] + 2 * off + 2] = np.array([nc], "<u2").view(np.uint8)
+            pg[offs["v"] + off * 64: offs["v"] + off * 64 + 64] = vp
+            pg[offs["s"] + 2 * off: offs["s"] + 2 * off + 2] = np.array([s], "<u2").view(np.uint8)
+            pg[offs["z"] + 2 * off: offs["z"] + 2 * off + 2] = np.array([z], "<u2").view(np.uint8)
+    assert np.array_equal(cache, expect)
