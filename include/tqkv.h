@@ -1,0 +1,160 @@
+/*
+ * tqkv.h -- C ABI of libtqkv: TurboQuant speculative-verify decode attention
+ * over a quantised paged KV cache, hand-written CUDA for sm_103a.
+ *
+ * The method ("spec-decode-intel-arc", bryanvine.github.io/turboquant-xpu,
+ * 2026-04-14):
+ *   - section "Context: TurboQuant, speculative decoding, and the gap": keys
+ *     are Walsh-Hadamard rotated and coded against a precomputed Lloyd-Max
+ *     codebook, values are uniform-scalar quantised with a scale and a zero;
+ *     the presets turboquant_k8v4 (FP8 keys, 4-bit values) and
+ *     turboquant_k3v4_nc (3-bit keys with norm correction, 4-bit values); the
+ *     three hot kernels are the fused store, decode stage 1 and the stage 2
+ *     reduction;
+ *   - section "Roofline": the cache is blocks x 16 tokens x Hk x slot, the
+ *     k8v4 slot is 196 bytes;
+ *   - section "Part 3: The fused Triton kernel": all N_spec draft queries of a
+ *     sequence are processed in one launch and share one K dequant per tile;
+ *   - section "Part 4: The causal correction": draft query n attends to
+ *     cached_len + n + 1 tokens;
+ *   and "sycl-three-attempts-arc-b70" (2026-04-15), section "Part 3:
+ *   joint_matrix + split-KV": NUM_KV_SPLITS partial attention per (b, h_q),
+ *   then a log-sum-exp reduction over the splits.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers into caller-owned memory; the
+ *     library never allocates, frees, synchronises or keeps per-call state.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *     only enqueued; results are ready when the stream reaches that point.
+ *   - Arguments are validated on the host before anything is launched.  On
+ *     error nothing is enqueued and a tq_status other than TQ_OK is returned;
+ *     no entry point aborts, throws or prints.
+ *   - Element types: fp16 = IEEE binary16, fp32 = IEEE binary32, all arrays
+ *     dense row-major (C order) in the index order written below.
+ *   - Head dimension D is 128 and the cache block (page) holds 16 tokens.
+ */
+#ifndef TQKV_H
+#define TQKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size   */
+  TQ_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement  */
+  TQ_ERR_MISALIGNED = 3,  /* a pointer lacks the alignment stated below    */
+  TQ_ERR_CUDA = 4,        /* the CUDA runtime reported a launch error      */
+  TQ_ERR_TIMEOUT = 5      /* reserved: a bounded device-side wait expired  */
+} tq_status;
+
+typedef enum {
+  TQ_PRESET_K8V4 = 0,    /* keys e4m3 (RNE, saturating), values 4-bit         */
+  TQ_PRESET_K3V4_NC = 1  /* keys: WHT + 3-bit Lloyd-Max codes + fp16 norm
+                            correction; values 4-bit                           */
+} tq_preset;
+
+/* Description of a caller-owned paged cache in device memory.
+ * Layout: u8 [num_blocks][num_kv_heads][tq_page_bytes(preset)].  One page is
+ * the 16 tokens of one block for one kv-head, stored planar:
+ *   k8v4    (3136 B = 16 x 196): K e4m3 [16][128] @0 | V nibbles [16][64] @2048
+ *           | V scale fp16 [16] @3072 | V zero fp16 [16] @3104
+ *   k3v4_nc (1920 B = 16 x 120): K codes [16][48] @0 | K nc fp16 [16] @768
+ *           | V nibbles [16][64] @800 | V scale fp16 [16] @1824
+ *           | V zero fp16 [16] @1856 | 32 B padding @1888 (never written)
+ * V nibble byte i of a token holds code 2i (low nibble) and 2i+1 (high); the
+ * 3-bit key codes form a little-endian bit stream, code j at bits 3j..3j+2.
+ * `cache` must be 16-byte aligned. */
+typedef struct {
+  int32_t preset;       /* tq_preset                                  */
+  int32_t head_dim;     /* must be 128                                */
+  int32_t block_size;   /* must be 16                                 */
+  int32_t num_kv_heads; /* Hk >= 1                                    */
+  int32_t num_blocks;   /* >= 0                                       */
+  int32_t reserved;     /* must be 0                                  */
+  void* cache;          /* device pointer, see layout above           */
+} tq_cache_desc;
+
+/* Bytes of one (block, kv-head) page: 3136 (k8v4), 1920 (k3v4_nc), 0 for an
+ * unknown preset.  16 x the slot size of the "Roofline" section (196 B for
+ * k8v4; 120 B for k3v4_nc). */
+size_t tq_page_bytes(int32_t preset);
+
+/* Bytes of the stage-1 partials for one call: partial_o (fp32
+ * [n_spec][B][Hq][num_kv_splits][128]) plus partial_lse (fp32
+ * [n_spec][B][Hq][num_kv_splits]).  0 if an argument is < 1. */
+size_t tq_partials_bytes(int32_t n_spec, int32_t B, int32_t Hq, int32_t num_kv_splits);
+
+/* The k3v4_nc key codebook: the 8-level Lloyd-Max quantiser of N(0, 1/128)
+ * ("Context" section: a precomputed Lloyd-Max codebook), derived in fp64 at
+ * first use and rounded to fp16; written ascending to the HOST array
+ * centroids_out[8] as the fp32 values of those fp16 numbers.  Returns
+ * TQ_ERR_UNSUPPORTED for k8v4 (no codebook), TQ_ERR_INVALID_ARG for NULL. */
+tq_status tq_codebook(int32_t preset, float* centroids_out);
+
+/* Static English text for a status code (never NULL). */
+const char* tq_status_string(int32_t status);
+
+/* Fused store ("Context" section: the fused store kernel): quantise and pack
+ * T new tokens into the cache.
+ *   k, v          fp16 [T][num_kv_heads][128], 16-byte aligned
+ *   slot_mapping  int32 [T], 4-byte aligned: slot = block * 16 + offset;
+ *                 a negative slot or one >= num_blocks * 16 skips that token
+ * Per token-head, k8v4 writes the e4m3 key bytes; k3v4_nc computes |k|, the
+ * rotation H k, the nearest centroid of each coordinate of H k / (|k| sqrt 128)
+ * and nc = |k| / |c_hat| (fp16).  Values (both presets): zero = min, scale =
+ * (max - min) / 15 rounded up to fp16, codes = rint((v - zero) / scale)
+ * clamped to [0, 15].  The bytes are a deterministic function of k and v
+ * (fixed fp32 operation order).  T == 0 enqueues nothing.  Two tokens mapped
+ * to the same slot race (the last write of either wins per byte). */
+tq_status tq_store(const tq_cache_desc* cache, const void* k, const void* v,
+                   const int32_t* slot_mapping, int32_t T, void* stream);
+
+/* Spec-verify stage 1 ("Part 3" / "Part 4" sections and split-KV of
+ * "sycl-three-attempts"): partial softmax attention of every draft query over
+ * one of num_kv_splits ranges of its sequence's cached tokens.
+ *   q             fp16 [n_spec][B][Hq][128], 16-byte aligned
+ *   block_table   int32 [B][max_blocks], 4-byte aligned: the cache block of
+ *                 each 16-token page of each sequence; an id outside
+ *                 [0, num_blocks) makes that page's tokens invisible
+ *   seq_lens      int32 [B], 4-byte aligned: tokens of each sequence in the
+ *                 cache, INCLUDING its n_spec draft tokens (clamped to
+ *                 [0, max_blocks * 16])
+ *   causal        1: draft n of sequence b sees positions < L_b - n_spec + n + 1
+ *                 (cached_len + n + 1 with cached_len = L_b - n_spec);
+ *                 0: every draft sees all L_b positions (parallel completion)
+ *   partial_o     fp32 [n_spec][B][Hq][num_kv_splits][128], 16-byte aligned
+ *   partial_lse   fp32 [n_spec][B][Hq][num_kv_splits], 4-byte aligned
+ * Query head h uses kv-head h / (Hq / num_kv_heads) (GQA).  Split s covers
+ * positions [s * c, (s + 1) * c) with c = 16 * ceil(ceil(L_b / S) / 16).  For
+ * each (n, b, h, s): partial_o = softmax-weighted mean of the decoded values
+ * over the visible positions of the split, partial_lse = ln(sum exp(score))
+ * with score = q . k_hat / sqrt(128); an empty range gives partial_o = 0 and
+ * partial_lse = -inf.  Requires 1 <= n_spec <= 16, Hq % num_kv_heads == 0,
+ * n_spec * Hq / num_kv_heads <= 128, 1 <= num_kv_splits <= 65535,
+ * B <= 65535. */
+tq_status tq_verify_stage1(const tq_cache_desc* cache, const void* q, const int32_t* block_table,
+                           int32_t max_blocks, const int32_t* seq_lens, int32_t n_spec, int32_t B,
+                           int32_t Hq, int32_t num_kv_splits, int32_t causal, float* partial_o,
+                           float* partial_lse, void* stream);
+
+/* Spec-verify stage 2 ("Roofline" section: the stage-2 reduction kernel):
+ * log-sum-exp merge of the splits,
+ *   out = sum_s exp(lse_s - M) o_s / sum_s exp(lse_s - M),  M = max_s lse_s,
+ * and out = 0 for a row whose splits are all empty.
+ *   partial_o, partial_lse  as written by tq_verify_stage1 (same alignment)
+ *   out                     fp32 [n_spec][B][Hq][128], 16-byte aligned
+ * head_dim must be 128. */
+tq_status tq_verify_stage2(const float* partial_o, const float* partial_lse, int32_t n_spec,
+                           int32_t B, int32_t Hq, int32_t head_dim, int32_t num_kv_splits,
+                           float* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQKV_H */

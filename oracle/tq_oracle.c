@@ -357,6 +357,7 @@ int oracle_store(int preset, uint8_t* cache, int num_blocks, int Hk, const uint1
   if (pb < 0) return -1;
   uint16_t cb[8];
   if (preset == PRESET_K3V4_NC) oracle_codebook16(cb);
+#pragma omp parallel for schedule(static)
   for (int t = 0; t < T; ++t) {
     int32_t slot = slot_mapping[t];
     if (slot < 0 || slot >= num_blocks * BLK) continue;

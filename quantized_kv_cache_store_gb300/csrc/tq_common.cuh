@@ -1,0 +1,76 @@
+// tq_common.cuh -- page layout, launch parameters and small device helpers
+// shared by the store and verify kernels of libtqkv (internal header).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tq {
+
+constexpr int kD = 128;      // head dimension
+constexpr int kBlock = 16;   // tokens per cache block (page)
+
+// Planar page of one (block, kv-head): the byte budgets of the two presets
+// (k8v4 slot 196 B as in the "Roofline" section of spec-decode-intel-arc;
+// k3v4_nc slot 118 B aligned to 120 B).
+struct K8 {
+  static constexpr int kKey = 0;      // e4m3 [16][128]
+  static constexpr int kVal = 2048;   // nibbles [16][64]
+  static constexpr int kScale = 3072; // fp16 [16]
+  static constexpr int kZero = 3104;  // fp16 [16]
+  static constexpr int kPage = 3136;
+};
+struct K3 {
+  static constexpr int kKey = 0;      // 3-bit codes [16][48]
+  static constexpr int kNc = 768;     // fp16 [16]
+  static constexpr int kVal = 800;    // nibbles [16][64]
+  static constexpr int kScale = 1824; // fp16 [16]
+  static constexpr int kZero = 1856;  // fp16 [16]
+  static constexpr int kPage = 1920;  // 32 B padding at 1888
+};
+
+// Eight fp16 centroids, ascending, passed to kernels by value.
+struct Codebook {
+  uint16_t c[8];
+};
+
+struct StoreArgs {
+  uint8_t* cache;
+  int num_blocks;
+  int Hk;
+  const __half* k;
+  const __half* v;
+  const int32_t* slots;
+  int T;
+  Codebook cb;
+};
+
+struct VerifyArgs {
+  const uint8_t* cache;
+  int num_blocks;
+  int Hk;
+  const __half* q;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* seq_lens;
+  int n_spec, B, Hq, group, R, S, causal;
+  float* part_o;
+  float* part_lse;
+  Codebook cb;
+};
+
+struct MergeArgs {
+  const float* part_o;
+  const float* part_lse;
+  float* out;
+  long rows;
+  int S;
+};
+
+// Host-side launchers (each returns the cudaError_t of its launch).
+cudaError_t launch_store(int preset, const StoreArgs& a, cudaStream_t st);
+cudaError_t launch_verify_stage1(int preset, const VerifyArgs& a, cudaStream_t st);
+cudaError_t launch_verify_stage2(const MergeArgs& a, cudaStream_t st);
+
+}  // namespace tq

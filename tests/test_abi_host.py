@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads and
+exports every declared entry point; helper values; argument validation rejects
+bad calls before anything is launched."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from quantized_kv_cache_store_gb300 import _build, tqkv
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "tqkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return tqkv.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"tq_store", "tq_verify_stage1", "tq_verify_stage2", "tq_page_bytes",
+            "tq_partials_bytes", "tq_codebook", "tq_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_page_and_partials_bytes(lib):
+    assert tqkv.tq_page_bytes(0) == 3136 and tqkv.tq_page_bytes(1) == 1920
+    assert tqkv.tq_page_bytes(7) == 0
+    assert tqkv.tq_partials_bytes(8, 4, 32, 8) == 8 * 4 * 32 * 8 * 129 * 4
+    assert tqkv.tq_partials_bytes(0, 4, 32, 8) == 0
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert tqkv.tq_status_string(s) and tqkv.tq_status_string(s) != "unknown status"
+    assert tqkv.tq_status_string(99) == "unknown status"
+
+
+def test_codebook_matches_oracle(lib, oracle_lib):
+    ours = tqkv.tq_codebook(1)
+    ref = oracle_lib.codebook16().view(np.float16).astype(np.float32)
+    assert np.array_equal(ours, ref)
+    out = np.zeros(8, np.float32)
+    assert lib.tq_codebook(0, ctypes.c_void_p(out.ctypes.data)) == tqkv.TQ_ERR_UNSUPPORTED
+    assert lib.tq_codebook(1, None) == tqkv.TQ_ERR_INVALID_ARG
+
+
+def _desc(preset=0, hk=4, nb=8, ptr=0x10000, head_dim=128, block=16, reserved=0):
+    return tqkv.tq_cache_desc(preset, head_dim, block, hk, nb, reserved, ptr)
+
+
+FAKE = 0x7f0000000000  # 16-byte aligned fake device address; never dereferenced on these paths
+
+
+def _s1(lib, d, q=FAKE, bt=FAKE, mb=4, sl=FAKE, n=8, B=1, Hq=32, S=2, causal=1, po=FAKE, pl=FAKE):
+    return lib.tq_verify_stage1(ctypes.byref(d) if d is not None else None, q, bt, mb, sl, n, B, Hq, S,
+                                causal, po, pl, None)
+
+
+def test_store_validation(lib):
+    P = ctypes.c_void_p
+    st = lambda d, k=FAKE, v=FAKE, s=FAKE, T=4: lib.tq_store(ctypes.byref(d) if d else None, P(k), P(v),
+                                                             P(s), T, None)
+    assert st(None) == tqkv.TQ_ERR_INVALID_ARG
+    assert st(_desc(ptr=0)) == tqkv.TQ_ERR_INVALID_ARG
+    assert st(_desc(preset=5, ptr=FAKE)) == tqkv.TQ_ERR_UNSUPPORTED
+    assert st(_desc(head_dim=64, ptr=FAKE)) == tqkv.TQ_ERR_UNSUPPORTED
+    assert st(_desc(block=32, ptr=FAKE)) == tqkv.TQ_ERR_UNSUPPORTED
+    assert st(_desc(hk=0, ptr=FAKE)) == tqkv.TQ_ERR_INVALID_ARG
+    assert st(_desc(reserved=1, ptr=FAKE)) == tqkv.TQ_ERR_INVALID_ARG
+    assert st(_desc(ptr=FAKE + 8)) == tqkv.TQ_ERR_MISALIGNED
+    assert st(_desc(ptr=FAKE), k=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert st(_desc(ptr=FAKE), k=FAKE + 2) == tqkv.TQ_ERR_MISALIGNED
+    assert st(_desc(ptr=FAKE), s=FAKE + 2) == tqkv.TQ_ERR_MISALIGNED
+    assert st(_desc(ptr=FAKE), T=-1) == tqkv.TQ_ERR_INVALID_ARG
+    assert st(_desc(ptr=FAKE), T=0) == tqkv.TQ_OK  # nothing to enqueue
+
+
+def test_stage1_validation(lib):
+    d = _desc(ptr=FAKE)
+    assert _s1(lib, None) == tqkv.TQ_ERR_INVALID_ARG
+    assert _s1(lib, d, q=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert _s1(lib, d, n=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert _s1(lib, d, n=17) == tqkv.TQ_ERR_UNSUPPORTED
+    assert _s1(lib, d, Hq=30) == tqkv.TQ_ERR_INVALID_ARG       # Hq % Hk != 0
+    assert _s1(lib, d, Hq=128) == tqkv.TQ_ERR_UNSUPPORTED      # 8 drafts x 32 heads per kv-head > 128 rows
+    assert _s1(lib, d, S=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert _s1(lib, d, S=70000) == tqkv.TQ_ERR_UNSUPPORTED
+    assert _s1(lib, d, causal=2) == tqkv.TQ_ERR_INVALID_ARG
+    assert _s1(lib, d, mb=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert _s1(lib, d, q=FAKE + 4) == tqkv.TQ_ERR_MISALIGNED
+    assert _s1(lib, d, po=FAKE + 4) == tqkv.TQ_ERR_MISALIGNED
+    assert _s1(lib, d, sl=FAKE + 1) == tqkv.TQ_ERR_MISALIGNED
+    assert _s1(lib, d, B=-1) == tqkv.TQ_ERR_INVALID_ARG
+    assert _s1(lib, d, B=0) == tqkv.TQ_OK  # nothing to enqueue
+
+
+def test_stage2_validation(lib):
+    s2 = lambda po=FAKE, pl=FAKE, n=8, B=1, Hq=8, D=128, S=2, out=FAKE: lib.tq_verify_stage2(
+        po, pl, n, B, Hq, D, S, out, None)
+    assert s2(po=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert s2(out=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert s2(S=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert s2(D=64) == tqkv.TQ_ERR_UNSUPPORTED
+    assert s2(out=FAKE + 4) == tqkv.TQ_ERR_MISALIGNED
+    assert s2(pl=FAKE + 2) == tqkv.TQ_ERR_MISALIGNED
