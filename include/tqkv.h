@@ -49,7 +49,7 @@ typedef enum {
   TQ_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement  */
   TQ_ERR_MISALIGNED = 3,  /* a pointer lacks the alignment stated below    */
   TQ_ERR_CUDA = 4,        /* the CUDA runtime reported a launch error      */
-  TQ_ERR_TIMEOUT = 5      /* reserved: a bounded device-side wait expired  */
+  TQ_ERR_TIMEOUT = 5      /* a bounded device-side wait expired            */
 } tq_status;
 
 typedef enum {
@@ -61,13 +61,15 @@ typedef enum {
 /* Description of a caller-owned paged cache in device memory.
  * Layout: u8 [num_blocks][num_kv_heads][tq_page_bytes(preset)].  One page is
  * the 16 tokens of one block for one kv-head, stored planar:
- *   k8v4    (3136 B = 16 x 196): K e4m3 [16][128] @0 | V nibbles [16][64] @2048
+ *   k8v4    (3136 B = 16 x 196): K e4m3 [16][128] @0 | V codes [128][8] @2048
  *           | V scale fp16 [16] @3072 | V zero fp16 [16] @3104
  *   k3v4_nc (1920 B = 16 x 120): K codes [16][48] @0 | K nc fp16 [16] @768
- *           | V nibbles [16][64] @800 | V scale fp16 [16] @1824
+ *           | V codes [128][8] @800 | V scale fp16 [16] @1824
  *           | V zero fp16 [16] @1856 | 32 B padding @1888 (never written)
- * V nibble byte i of a token holds code 2i (low nibble) and 2i+1 (high); the
- * 3-bit key codes form a little-endian bit stream, code j at bits 3j..3j+2.
+ * V codes are coordinate-major: byte 8d + t/2 holds the 4-bit code of
+ * coordinate d for token t of the page (low nibble for even t).  The 3-bit
+ * key codes of a token form a little-endian bit stream, code j at bits
+ * 3j..3j+2.
  * `cache` must be 16-byte aligned. */
 typedef struct {
   int32_t preset;       /* tq_preset                                  */
@@ -152,6 +154,15 @@ tq_status tq_verify_stage1(const tq_cache_desc* cache, const void* q, const int3
 tq_status tq_verify_stage2(const float* partial_o, const float* partial_lse, int32_t n_spec,
                            int32_t B, int32_t Hq, int32_t head_dim, int32_t num_kv_splits,
                            float* out, void* stream);
+
+/* Reads and clears the library's sticky device-side error word on the
+ * current device.  Every wait of the tensor-core stage-1 kernel on a shared
+ * memory barrier is bounded; when one expires the kernel gives up on its
+ * (split, kv-head, sequence), writes NaN partials for it and sets the word.
+ * Returns TQ_ERR_TIMEOUT if that happened since the last call, TQ_OK if not,
+ * TQ_ERR_CUDA if the word could not be read.  Synchronises the device (it is
+ * a diagnostic, not a per-call step). */
+tq_status tq_device_status(void);
 
 #ifdef __cplusplus
 }

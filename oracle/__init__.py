@@ -199,8 +199,9 @@ def encode_key8(k) -> np.ndarray:
 
 
 def encode_value4(v) -> tuple[np.ndarray, int, int]:
+    """Returns (codes uint8[128] in 0..15, scale fp16 bits, zero fp16 bits)."""
     v = _u16(v)
-    out = np.zeros(64, np.uint8)
+    out = np.zeros(HEAD_DIM, np.uint8)
     s = np.zeros(1, np.uint16)
     z = np.zeros(1, np.uint16)
     _load().oracle_encode_value4(_ptr(v), _ptr(out), _ptr(s), _ptr(z))

@@ -32,8 +32,9 @@
  *     up to fp16, codes rounded half-to-even and clamped to [0, 15];
  *   - FP8 keys: e4m3, round-to-nearest-even, saturating to +-448, NaN -> 0x7F,
  *     no scale and no rotation;
- *   - bit order: 3-bit codes LSB-first in a little-endian stream, low nibble
- *     first for values; the page for one (block, kv-head) is planar (below).
+ *   - bit order: 3-bit codes LSB-first in a little-endian stream; value codes
+ *     coordinate-major (byte 8d + t/2, low nibble = even token t); the page for
+ *     one (block, kv-head) is planar (below).
  *
  * Arithmetic: the encoder is fp32 in a fixed operation order (this file must be
  * compiled with -ffp-contract=off and without -ffast-math); the attention part
@@ -49,7 +50,8 @@
 
 enum { PRESET_K8V4 = 0, PRESET_K3V4_NC = 1 };
 
-/* Planar page layout for one (block, kv-head), 16 tokens.  Byte budgets:
+/* Planar page layout for one (block, kv-head), 16 tokens (value codes stored
+ * coordinate-major: 128 coordinates x 8 bytes of 16 nibbles).  Byte budgets:
  * k8v4 slot = 128 (K) + 64 (V codes) + 2 (scale) + 2 (zero) = 196 B, which is
  * the slot_size_aligned the [SD] "Roofline" section multiplies out;
  * k3v4_nc slot = 48 (codes) + 2 (nc) + 64 + 2 + 2 = 118 B, aligned to 120 B,
@@ -316,9 +318,9 @@ void oracle_encode_key8(const uint16_t k[D], uint8_t out[D]) {
 }
 
 /* 4-bit value encoder for one token-head ([SD] "Context": uniform scalar
- * quantisation of values with a scale and a zero).  Writes 64 nibble bytes
- * (low nibble = even coordinate) and the fp16 scale and zero. */
-void oracle_encode_value4(const uint16_t v[D], uint8_t out[64], uint16_t* scale_out,
+ * quantisation of values with a scale and a zero).  Writes the 128 codes (one
+ * per byte, 0..15) and the fp16 scale and zero. */
+void oracle_encode_value4(const uint16_t v[D], uint8_t code[D], uint16_t* scale_out,
                           uint16_t* zero_out) {
   float lo = oracle_h2f(v[0]), hi = lo;
   for (int j = 1; j < D; ++j) {
@@ -334,7 +336,6 @@ void oracle_encode_value4(const uint16_t v[D], uint8_t out[64], uint16_t* scale_
     if (oracle_h2f(sh) < r) sh = (uint16_t)(sh + 1); /* round the scale up */
   }
   float zf = oracle_h2f(zh), sf = oracle_h2f(sh);
-  uint8_t code[D];
   for (int j = 0; j < D; ++j) {
     int c = 0;
     if (sh != 0) {
@@ -343,9 +344,23 @@ void oracle_encode_value4(const uint16_t v[D], uint8_t out[64], uint16_t* scale_
     }
     code[j] = (uint8_t)c;
   }
-  for (int i = 0; i < 64; ++i) out[i] = (uint8_t)(code[2 * i] | (code[2 * i + 1] << 4));
   *scale_out = sh;
   *zero_out = zh;
+}
+
+/* Value codes in a page are stored coordinate-major: byte 8 * d + off / 2 of
+ * the value region holds the code of coordinate d for token off (low nibble
+ * for even off, high nibble for odd off). */
+static void put_value_codes(uint8_t* vregion, int off, const uint8_t code[D]) {
+  for (int d = 0; d < D; ++d) {
+    uint8_t* b = vregion + 8 * d + off / 2;
+    int sh = 4 * (off % 2);
+    *b = (uint8_t)((*b & ~(0xF << sh)) | (code[d] << sh));
+  }
+}
+
+static int get_value_code(const uint8_t* vregion, int off, int d) {
+  return (vregion[8 * d + off / 2] >> (4 * (off % 2))) & 15;
 }
 
 /* Store T new tokens into the paged cache [num_blocks][Hk][page].  k, v are
@@ -357,26 +372,30 @@ int oracle_store(int preset, uint8_t* cache, int num_blocks, int Hk, const uint1
   if (pb < 0) return -1;
   uint16_t cb[8];
   if (preset == PRESET_K3V4_NC) oracle_codebook16(cb);
+  /* heads own disjoint pages, so they can be encoded in parallel; tokens of
+   * one head share value-code bytes and are encoded in order */
 #pragma omp parallel for schedule(static)
-  for (int t = 0; t < T; ++t) {
-    int32_t slot = slot_mapping[t];
-    if (slot < 0 || slot >= num_blocks * BLK) continue;
-    int blk = slot / BLK, off = slot % BLK;
-    for (int h = 0; h < Hk; ++h) {
+  for (int h = 0; h < Hk; ++h) {
+    for (int t = 0; t < T; ++t) {
+      int32_t slot = slot_mapping[t];
+      if (slot < 0 || slot >= num_blocks * BLK) continue;
+      int blk = slot / BLK, off = slot % BLK;
       uint8_t* page = cache + ((long)blk * Hk + h) * pb;
       const uint16_t* kk = k + ((long)t * Hk + h) * D;
       const uint16_t* vv = v + ((long)t * Hk + h) * D;
       uint16_t s, z;
+      uint8_t code[D];
+      oracle_encode_value4(vv, code, &s, &z);
       if (preset == PRESET_K8V4) {
         oracle_encode_key8(kk, page + K8_K_OFF + off * D);
-        oracle_encode_value4(vv, page + K8_V_OFF + off * 64, &s, &z);
+        put_value_codes(page + K8_V_OFF, off, code);
         put_h(page + K8_S_OFF + 2 * off, s);
         put_h(page + K8_Z_OFF + 2 * off, z);
       } else {
         uint16_t nc;
         oracle_encode_key3(kk, cb, page + K3_K_OFF + off * 48, &nc);
         put_h(page + K3_NC_OFF + 2 * off, nc);
-        oracle_encode_value4(vv, page + K3_V_OFF + off * 64, &s, &z);
+        put_value_codes(page + K3_V_OFF, off, code);
         put_h(page + K3_S_OFF + 2 * off, s);
         put_h(page + K3_Z_OFF + 2 * off, z);
       }
@@ -411,11 +430,7 @@ void oracle_decode_value(int preset, const uint8_t* page, int off, double out[D]
   int zo = preset == PRESET_K8V4 ? K8_Z_OFF : K3_Z_OFF;
   double s = (double)oracle_h2f(get_h(page + so + 2 * off));
   double z = (double)oracle_h2f(get_h(page + zo + 2 * off));
-  for (int i = 0; i < 64; ++i) {
-    uint8_t byte = page[vo + off * 64 + i];
-    out[2 * i] = (double)(byte & 15) * s + z;
-    out[2 * i + 1] = (double)(byte >> 4) * s + z;
-  }
+  for (int j = 0; j < D; ++j) out[j] = (double)get_value_code(page + vo, off, j) * s + z;
 }
 
 /* -------------------------------------------------------------- attention */

@@ -163,8 +163,17 @@ __device__ __forceinline__ void store_value4(uint8_t* page, int off, int lane, c
     qv = fminf(fmaxf(qv, 0.0f), 15.0f);
     c[i] = (uint32_t)qv;
   }
-  const uint16_t packed = (uint16_t)((c[0] | (c[1] << 4)) | ((c[2] | (c[3] << 4)) << 8));
-  *reinterpret_cast<uint16_t*>(page + L::kVal + off * 64 + 2 * lane) = packed;
+  // codes are stored coordinate-major: byte 8d + off/2, low nibble = even off.
+  // Tokens of one page share bytes, so each nibble is replaced atomically.
+  uint32_t* vw = reinterpret_cast<uint32_t*>(page + L::kVal);
+  const int nib = 4 * (off & 7);
+  const uint32_t keep = ~(0xFu << nib);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t* w = vw + 2 * (4 * lane + i) + (off >> 3);
+    atomicAnd(w, keep);
+    atomicOr(w, c[i] << nib);
+  }
   if (lane == 0) {
     *reinterpret_cast<uint16_t*>(page + L::kScale + 2 * off) = sh;
     *reinterpret_cast<uint16_t*>(page + L::kZero + 2 * off) = __half_as_ushort(zh);

@@ -16,7 +16,7 @@ constexpr int kBlock = 16;   // tokens per cache block (page)
 // k3v4_nc slot 118 B aligned to 120 B).
 struct K8 {
   static constexpr int kKey = 0;      // e4m3 [16][128]
-  static constexpr int kVal = 2048;   // nibbles [16][64]
+  static constexpr int kVal = 2048;   // codes [128 coord][8 B: 16 tokens]
   static constexpr int kScale = 3072; // fp16 [16]
   static constexpr int kZero = 3104;  // fp16 [16]
   static constexpr int kPage = 3136;
@@ -24,11 +24,18 @@ struct K8 {
 struct K3 {
   static constexpr int kKey = 0;      // 3-bit codes [16][48]
   static constexpr int kNc = 768;     // fp16 [16]
-  static constexpr int kVal = 800;    // nibbles [16][64]
+  static constexpr int kVal = 800;    // codes [128 coord][8 B: 16 tokens]
   static constexpr int kScale = 1824; // fp16 [16]
   static constexpr int kZero = 1856;  // fp16 [16]
   static constexpr int kPage = 1920;  // 32 B padding at 1888
 };
+
+template <int PRESET>
+struct Layout;
+template <>
+struct Layout<0> : K8 {};
+template <>
+struct Layout<1> : K3 {};
 
 // Eight fp16 centroids, ascending, passed to kernels by value.
 struct Codebook {
@@ -72,5 +79,10 @@ struct MergeArgs {
 cudaError_t launch_store(int preset, const StoreArgs& a, cudaStream_t st);
 cudaError_t launch_verify_stage1(int preset, const VerifyArgs& a, cudaStream_t st);
 cudaError_t launch_verify_stage2(const MergeArgs& a, cudaStream_t st);
+// tensor-core stage 1 (tcgen05), used for up to 64 query rows per kv-head
+bool verify_stage1_tc_supported(const VerifyArgs& a);
+cudaError_t launch_verify_stage1_tc(int preset, const VerifyArgs& a, cudaStream_t st);
+// sticky device-side error word (nonzero after a bounded wait expired)
+cudaError_t read_device_error(unsigned int* out, bool clear);
 
 }  // namespace tq

@@ -180,4 +180,10 @@ tq_status tq_verify_stage2(const float* partial_o, const float* partial_lse, int
   return from_cuda(tq::launch_verify_stage2(a, static_cast<cudaStream_t>(stream)));
 }
 
+tq_status tq_device_status(void) {
+  unsigned int word = 0;
+  if (tq::read_device_error(&word, true) != cudaSuccess) return TQ_ERR_CUDA;
+  return word ? TQ_ERR_TIMEOUT : TQ_OK;
+}
+
 }  // extern "C"

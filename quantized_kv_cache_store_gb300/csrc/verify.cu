@@ -67,24 +67,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t w) {
   return (uint32_t)r.x | ((uint32_t)r.y << 16);
 }
 
-// nibble pairs: low half = nibble of xa, high half = same nibble of xb, as
-// exact fp16 integers 0..15.  `byte` selects the byte of the 32-bit words,
-// `hi` the nibble inside it.
-__device__ __forceinline__ uint32_t nib2_to_half2(uint32_t xa, uint32_t xb, int byte, bool hi) {
-  uint32_t y = __byte_perm(xa, xb, (uint32_t)byte | ((uint32_t)(4 + byte) << 8));
-  if (hi) y >>= 4;
-  const uint32_t magic = (y & 0x000F000Fu) | 0x64006400u;  // 1024 + n in each half
+// one byte of value codes (two consecutive tokens of one coordinate: low
+// nibble = even token) -> f16x2 of the two codes as exact integers 0..15
+__device__ __forceinline__ uint32_t codepair_to_half2(uint32_t w, int byte) {
+  const uint32_t b = (w >> (8 * byte)) & 0xFFu;
+  const uint32_t magic = (b & 0xFu) | ((b & 0xF0u) << 12) | 0x64006400u;  // 1024 + n per half
   const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&magic),
                             __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
-
-template <int PRESET>
-struct Layout;
-template <>
-struct Layout<0> : K8 {};
-template <>
-struct Layout<1> : K3 {};
 
 template <int PAGE, int TW>
 struct Ring {
@@ -379,19 +370,14 @@ __global__ void __launch_bounds__(RW* TW * 32, 1) verify_stage1_kernel(VerifyArg
       pf[2] = pack_half2(pA[1][0], pA[1][1]);
       pf[3] = pack_half2(pB[1][0], pB[1][1]);
 
-      // ---- O += P V: B fragment column n = g is coordinate 16g + dt
-      const uint8_t* vr = pg + L::kVal + 8 * g;
-      const uint2 x0 = *reinterpret_cast<const uint2*>(vr + (2 * c) * 64);
-      const uint2 x1 = *reinterpret_cast<const uint2*>(vr + (2 * c + 1) * 64);
-      const uint2 x2 = *reinterpret_cast<const uint2*>(vr + (2 * c + 8) * 64);
-      const uint2 x3 = *reinterpret_cast<const uint2*>(vr + (2 * c + 9) * 64);
+      // ---- O += P V: B fragment column n = g is coordinate d = 16g + dt; its
+      // codes for tokens (2c, 2c+1) are byte c of the coordinate's 8-byte row,
+      // for tokens (2c+8, 2c+9) byte 4 + c
+      const uint2* vr = reinterpret_cast<const uint2*>(pg + L::kVal + 8 * 16 * g);
 #pragma unroll
       for (int dt = 0; dt < 16; ++dt) {
-        const int byte = (dt >> 1) & 3;
-        const bool hi = dt & 1;
-        const uint32_t ua = dt < 8 ? x0.x : x0.y, ub = dt < 8 ? x1.x : x1.y;
-        const uint32_t uc = dt < 8 ? x2.x : x2.y, ud = dt < 8 ? x3.x : x3.y;
-        mma16816(acc[dt], pf, nib2_to_half2(ua, ub, byte, hi), nib2_to_half2(uc, ud, byte, hi));
+        const uint2 row = vr[dt];
+        mma16816(acc[dt], pf, codepair_to_half2(row.x, c), codepair_to_half2(row.y, c));
       }
     }
     __syncthreads();
@@ -551,6 +537,7 @@ cudaError_t launch_s1_rows(const VerifyArgs& a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_verify_stage1(int preset, const VerifyArgs& a, cudaStream_t st) {
+  if (verify_stage1_tc_supported(a)) return launch_verify_stage1_tc(preset, a, st);
   return preset == 0 ? launch_s1_rows<0>(a, st) : launch_s1_rows<1>(a, st);
 }
 

@@ -1,0 +1,677 @@
+// verify_tc.cu -- spec-verify stage 1 on the sm_103a tensor cores (tcgen05,
+// tensor memory, bulk copies, mbarriers), for up to 64 query rows per kv-head.
+//
+// Method ("spec-decode-intel-arc", sections "Part 3: The fused Triton
+// kernel" and "Part 4: The causal correction"; split-KV of
+// "sycl-three-attempts-arc-b70", section "Part 3"): for one (split, kv-head,
+// sequence) every draft x GQA query row attends to the split's visible cache
+// tokens with an online softmax; one dequantisation of each cache tile serves
+// all rows.
+//
+// Work is cut into chunks of 128 tokens (8 pages).  Both contractions are
+// transposed so that the 128-row side of the MMA is tokens or coordinates:
+//   S^T[token, row]  = K_hat[token, :] . Q[row, :]         (M = 128, N = rows)
+//   O^T[d, row]     += V_codes^T[d, token] . P'[row, token] (M = 128, N = rows)
+// with A operands in tensor memory (written by the dequantising threads with
+// tcgen05.st) and B operands in shared memory (Q once per CTA; P' per chunk).
+//   keys   : k8v4 e4m3 -> f16 exactly; k3v4_nc 3-bit code pairs -> fp16
+//            centroid pairs through a per-lane replicated table; the norm
+//            correction nc_t scales token t's scores (its TMEM lane) after the
+//            MMA; the query is rotated once, q_rot = H q / sqrt(D).
+//   values : codes enter as exact fp16 integers; P' = p * scale_t; the zero
+//            term sum_t p_t zero_t and l = sum_t p_t are kept per thread in
+//            fp32 and reduced once at the end.
+// Softmax: thread t owns token t (its S^T lane) and 32 query rows.  The
+// running maximum is updated lazily: only when some score exceeds it by more
+// than 8 (log2 units) is the exact chunk maximum computed across the 128
+// tokens and O^T, l and the zero term rescaled; otherwise probabilities stay
+// bounded by 2^8 and the stale maximum is used (any reference point gives the
+// same softmax).
+//
+// Warp roles: warp 0 = bulk-copy producer, warp 1 = MMA issuer, warp 2 = TMEM
+// owner; warpgroup 1 = dequantisation (thread i: token i for keys, coordinate
+// i for values); warpgroups 2.. = softmax (32 rows each).  Every wait on an
+// mbarrier is bounded: on expiry the CTA sets an abort flag and the sticky
+// device error word, drains its in-flight copies and MMAs, frees its tensor
+// memory and writes NaN partials.
+#include <math_constants.h>
+
+#include <atomic>
+
+#include <cuda_fp8.h>
+
+#include "tc_ptx.cuh"
+#include "tq_common.cuh"
+
+namespace tq {
+
+__device__ unsigned int g_tq_device_error;  // sticky: nonzero after a bounded wait expired
+
+namespace {
+
+using namespace ptx;
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint32_t kSpinLimit = 1u << 24;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
+
+constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+template <int PRESET, int NMMA>
+struct Cfg {
+  using L = Layout<PRESET>;
+  static constexpr int kTok = 128;  // tokens per chunk
+  static constexpr int kPages = 8;  // pages per chunk
+  static constexpr int kStageBytes = kPages * L::kPage;
+  static constexpr int kStages = PRESET == 0 ? 4 : 6;
+  static constexpr int kSW = NMMA == 64 ? 2 : 1;  // softmax warpgroups
+  static constexpr int kNC = NMMA / kSW;          // columns (rows of Q) per softmax thread
+  static constexpr int kThreads = 256 + 128 * kSW;
+  // per-thread register budgets after setmaxnreg (control / dequant / softmax);
+  // their sum over the warpgroups must stay within what the launch granted
+  static constexpr int kRegCtl = kSW == 2 ? 32 : 48, kRegDeq = kSW == 2 ? 80 : 112, kRegSm = kSW == 2 ? 192 : 232;
+  static constexpr int kRegNeeded = 128 * (kRegCtl + kRegDeq + kSW * kRegSm);
+  static constexpr int kLine = 2 * NMMA;  // bytes of one P' line (one token)
+  static constexpr int kSwzBits = NMMA == 64 ? 3 : (NMMA == 32 ? 2 : 1);
+  static constexpr uint32_t kSwzMode = NMMA == 64 ? 2u : (NMMA == 32 ? 4u : 6u);
+  // shared memory (offsets from a 1024-byte aligned base)
+  static constexpr int kRing = 0;
+  static constexpr int kQ = align_up(kStages * kStageBytes, 1024);
+  static constexpr int kQBytes = 2 * NMMA * 128;  // K-major, 128B swizzle, 2 x 64-coordinate blocks
+  static constexpr int kP = kQ + align_up(kQBytes, 1024);
+  static constexpr int kPBytes = kTok * kLine;  // one buffer
+  static constexpr int kCol = kP + 2 * kPBytes;  // float4 [2][128]: column scale, v scale, v zero, row mask
+  static constexpr int kRed = kCol + 2 * kTok * 16;  // float [kSW][3][4][kNC]
+  static constexpr int kPair = kRed + kSW * 3 * 4 * kNC * 4;  // u32 [64][32] (k3v4_nc)
+  static constexpr int kPValid = kPair + (PRESET == 1 ? 64 * 32 * 4 : 0);  // u8 [kStages][8]
+  static constexpr int kBar = align_up(kPValid + kStages * 8, 8);
+  // full[kStages] empty[kStages] akv[2] qk[2] sfree[2] pfull[2] pv[2]
+  static constexpr int kNumBars = 2 * kStages + 10;
+  static constexpr int kMisc = kBar + 8 * kNumBars;  // u32 tmem base, u32 abort
+  static constexpr int kSmem = kMisc + 16 + 1024;    // + alignment slack
+  // tensor memory columns
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTAK = 0;     // A_K[2]: 64 cols each (token lanes, coordinate pairs)
+  static constexpr uint32_t kTAV = 128;   // A_V[2]: 64 cols each (coordinate lanes, token pairs)
+  static constexpr uint32_t kTS = 256;    // S^T[2]: NMMA cols each
+  static constexpr uint32_t kTO = 256 + 2 * NMMA;  // O^T: NMMA cols
+  static_assert(kTO + NMMA <= kTmemCols, "tensor memory overflow");
+  static_assert(kSmem <= 227 * 1024, "shared memory overflow");
+};
+
+struct Bars {
+  uint32_t base;
+  int stages;
+  __device__ uint32_t full(int s) const { return base + 8 * s; }
+  __device__ uint32_t empty(int s) const { return base + 8 * (stages + s); }
+  __device__ uint32_t akv(int b) const { return base + 8 * (2 * stages + b); }
+  __device__ uint32_t qk(int b) const { return base + 8 * (2 * stages + 2 + b); }
+  __device__ uint32_t sfree(int b) const { return base + 8 * (2 * stages + 4 + b); }
+  __device__ uint32_t pfull(int b) const { return base + 8 * (2 * stages + 6 + b); }
+  __device__ uint32_t pv(int b) const { return base + 8 * (2 * stages + 8 + b); }
+};
+
+// Bounded wait; false when the CTA aborted or this wait expired (which aborts).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
+                                         bool honour_abort = true) {
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (honour_abort && (i & 63u) == 63u && *abort) return false;
+    if (i >= kSpinLimit) {
+      *abort = 1u;
+      atomicOr(&g_tq_device_error, 1u);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t w16) {
+  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w16 & 0xFFFFu), __NV_E4M3);
+  return (uint32_t)r.x | ((uint32_t)r.y << 16);
+}
+
+// byte of value codes (tokens 2k, 2k+1 of one coordinate) -> f16x2 integers
+__device__ __forceinline__ uint32_t codebyte_to_half2(uint32_t b) {
+  const uint32_t magic = (b & 0xFu) | ((b & 0xF0u) << 12) | 0x64006400u;
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&magic),
+                            __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Reduce NC values per lane across the 32 lanes of a warp; afterwards lane l
+// holds the reduction of column (l % NC) in v[0].
+template <int NC, bool MAX>
+__device__ __forceinline__ void warp_transpose_reduce(float (&v)[NC], int lane) {
+#pragma unroll
+  for (int o = NC / 2; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = up ? v[i] : v[i + o];
+      const float keep = up ? v[i + o] : v[i];
+      const float recv = __shfl_xor_sync(kFull, send, o);
+      v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  if (NC < 32) {
+#pragma unroll
+    for (int o = 16; o >= NC; o >>= 1) {
+      const float recv = __shfl_xor_sync(kFull, v[0], o);
+      v[0] = MAX ? fmaxf(v[0], recv) : v[0] + recv;
+    }
+  }
+}
+
+template <int PRESET, int NMMA>
+__global__ void __launch_bounds__(Cfg<PRESET, NMMA>::kThreads, 1) verify_stage1_tc_kernel(VerifyArgs a) {
+  using C = Cfg<PRESET, NMMA>;
+  using L = typename C::L;
+  constexpr int kNC = C::kNC;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(sm);
+  uint8_t* pvalid = sm + C::kPValid;
+  float4* colp = reinterpret_cast<float4*>(sm + C::kCol);
+  float* red = reinterpret_cast<float*>(sm + C::kRed);
+  uint32_t* pairs = reinterpret_cast<uint32_t*>(sm + C::kPair);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kMisc);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sm + C::kMisc + 4);
+  const Bars bars{sbase + C::kBar, C::kStages};
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+
+  // ---- this split's token range
+  int L_b = a.seq_lens[b];
+  L_b = max(0, min(L_b, a.max_blocks * kBlock));
+  const int per = (L_b + a.S - 1) / a.S;
+  const int chunk = kBlock * ((per + kBlock - 1) / kBlock);
+  const int t_lo = split * chunk;
+  const int t_hi = min(t_lo + chunk, L_b);
+  const int page_lo = t_lo / kBlock;
+  const int npages = t_hi > t_lo ? (t_hi - t_lo + kBlock - 1) / kBlock : 0;
+  const int nchunks = (npages + C::kPages - 1) / C::kPages;
+  const int32_t* bt = a.block_table + (long)b * a.max_blocks;
+
+  // ---- set-up: barriers, tensor memory, query rows, code-pair table
+  if (tid == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bars.full(s), 1);
+      mbar_init(bars.empty(s), 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars.akv(i), 4);
+      mbar_init(bars.qk(i), 1);
+      mbar_init(bars.sfree(i), 4 * C::kSW);
+      mbar_init(bars.pfull(i), 4 * C::kSW);
+      mbar_init(bars.pv(i), 1);
+    }
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  {
+    // Q rows r = n * group + j (zero beyond R) into the K-major, 128B-swizzled
+    // B operand: row r, coordinate d at block d/64, line r, 16-byte chunk
+    // ((d % 64) / 8) ^ (r % 8).  k3v4_nc rotates: q_rot = H q / sqrt(128).
+    const int nwarps = C::kThreads / 32;
+    for (int r = warp; r < NMMA; r += nwarps) {
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      if (r < a.R) {
+        const int n = r / a.group, j = r % a.group;
+        const __half* qp = a.q + (((long)n * a.B + b) * a.Hq + kvh * a.group + j) * kD + 4 * lane;
+        const uint2 raw = *reinterpret_cast<const uint2*>(qp);
+        const __half2 h0 = *reinterpret_cast<const __half2*>(&raw.x);
+        const __half2 h1 = *reinterpret_cast<const __half2*>(&raw.y);
+        x[0] = __low2float(h0);
+        x[1] = __high2float(h0);
+        x[2] = __low2float(h1);
+        x[3] = __high2float(h1);
+      }
+      if (PRESET == 1) {
+        float u = x[0], v = x[1];
+        x[0] = u + v;
+        x[1] = u - v;
+        u = x[2];
+        v = x[3];
+        x[2] = u + v;
+        x[3] = u - v;
+        u = x[0];
+        v = x[2];
+        x[0] = u + v;
+        x[2] = u - v;
+        u = x[1];
+        v = x[3];
+        x[1] = u + v;
+        x[3] = u - v;
+#pragma unroll
+        for (int o = 1; o <= 16; o <<= 1) {
+          const bool upper = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float p = __shfl_xor_sync(kFull, x[i], o);
+            x[i] = upper ? p - x[i] : x[i] + p;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] *= 0.08838834764831845f;
+      }
+      const int kb = lane >> 4, chunk16 = (lane & 15) >> 1;
+      uint8_t* dst = sm + C::kQ + kb * (NMMA * 128) + (r >> 3) * 1024 + (r & 7) * 128 +
+                     ((chunk16 ^ (r & 7)) << 4) + 8 * (lane & 1);
+      uint2 out;
+      out.x = pack_half2(x[0], x[1]);
+      out.y = pack_half2(x[2], x[3]);
+      *reinterpret_cast<uint2*>(dst) = out;
+    }
+    if (PRESET == 1) {
+      for (int i = tid; i < 64 * 32; i += C::kThreads) {
+        const int e = i >> 5;
+        pairs[i] = (uint32_t)a.cb.c[e & 7] | ((uint32_t)a.cb.c[e >> 3] << 16);
+      }
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const float sl2 = kLog2e * 0.08838834764831845f;  // log2(e) / sqrt(128)
+
+  if (warp < 4) {
+    regs_dec<C::kRegCtl>();
+    if (warp == 0 && lane == 0) {
+      // ================= producer: 8 pages per chunk into the ring
+      int issued = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        const int st = c % C::kStages;
+        if (c >= C::kStages && !wait_bar(bars.empty(st), ((c / C::kStages) - 1) & 1, abort_flag)) break;
+        int blk[C::kPages];
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int p = 0; p < C::kPages; ++p) {
+          const int lp = c * C::kPages + p;
+          blk[p] = -1;
+          if (lp < npages) {
+            const int id = bt[page_lo + lp];
+            if (id >= 0 && id < a.num_blocks) blk[p] = id;
+          }
+          pvalid[st * 8 + p] = blk[p] >= 0 ? 1 : 0;
+          bytes += blk[p] >= 0 ? (uint32_t)L::kPage : 0u;
+        }
+        mbar_arrive_expect_tx(bars.full(st), bytes);
+#pragma unroll
+        for (int p = 0; p < C::kPages; ++p) {
+          if (blk[p] >= 0) {
+            const uint8_t* src = a.cache + ((long)blk[p] * a.Hk + kvh) * L::kPage;
+            bulk_g2s(sbase + C::kRing + st * C::kStageBytes + p * L::kPage, src, L::kPage, bars.full(st));
+          }
+        }
+        issued = c + 1;
+      }
+      // drain: copies still in flight must land before the CTA can exit
+      for (int c = max(0, issued - C::kStages); c < issued; ++c)
+        wait_bar(bars.full(c % C::kStages), (c / C::kStages) & 1, abort_flag, false);
+    } else if (warp == 1 && lane == 0) {
+      // ================= MMA issuer
+      constexpr uint32_t id_qk = idesc_f16(128, NMMA, 0, 0);
+      constexpr uint32_t id_pv = idesc_f16(128, NMMA, 0, 1);
+      int last_qk = -1, last_pv = -1;
+      auto issue_pv = [&](int cc) -> bool {
+        const int bb = cc & 1;
+        if (!wait_bar(bars.pfull(bb), (cc >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bd = smem_desc(sbase + C::kP + bb * C::kPBytes + kk * 16 * C::kLine, 16, 8 * C::kLine,
+                                        C::kSwzMode);
+          mma_ts(tmem + C::kTO, tmem + C::kTAV + 64 * bb + 8 * kk, bd, id_pv, (cc > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(bars.pv(bb));
+        last_pv = cc;
+        return true;
+      };
+      bool ok = true;
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int bb = c & 1;
+        if (!wait_bar(bars.akv(bb), (c >> 1) & 1, abort_flag)) break;
+        if (c >= 2 && !wait_bar(bars.sfree(bb), ((c - 2) >> 1) & 1, abort_flag)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bd = smem_desc(sbase + C::kQ + (kk >> 2) * (NMMA * 128) + (kk & 3) * 32, 16, 1024, 2);
+          mma_ts(tmem + C::kTS + NMMA * bb, tmem + C::kTAK + 64 * bb + 8 * kk, bd, id_qk, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bars.qk(bb));
+        last_qk = c;
+        if (c >= 1) ok = issue_pv(c - 1);
+      }
+      if (ok && last_qk == nchunks - 1 && nchunks > 0) issue_pv(nchunks - 1);
+      // drain the MMAs this thread issued before tensor memory is freed
+      if (last_qk >= 0) wait_bar(bars.qk(last_qk & 1), (last_qk >> 1) & 1, abort_flag, false);
+      if (last_pv >= 0) wait_bar(bars.pv(last_pv & 1), (last_pv >> 1) & 1, abort_flag, false);
+    }
+  } else if (warp < 8) {
+    regs_dec<C::kRegDeq>();
+    // ================= dequantisation: thread i = token i (keys), coordinate i (values)
+    const int i = tid - 128;
+    const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
+    const int pg_i = i >> 4, off = i & 15;
+    for (int c = 0; c < nchunks; ++c) {
+      const int st = c % C::kStages, bb = c & 1;
+      if (!wait_bar(bars.full(st), (c / C::kStages) & 1, abort_flag)) break;
+      if (c >= 2 && !wait_bar(bars.qk(bb), ((c - 2) >> 1) & 1, abort_flag)) break;
+      const uint8_t* stage = sm + C::kRing + st * C::kStageBytes;
+      const uint8_t* pg = stage + pg_i * L::kPage;
+      // ---- keys of token i -> A_K[bb], lane i, columns = coordinate pairs
+      if constexpr (PRESET == 0) {
+        const uint4* kr = reinterpret_cast<const uint4*>(pg + L::kKey + off * kD);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r[32];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 w = kr[4 * h + q];
+            r[8 * q + 0] = e4m3x2_to_half2(w.x);
+            r[8 * q + 1] = e4m3x2_to_half2(w.x >> 16);
+            r[8 * q + 2] = e4m3x2_to_half2(w.y);
+            r[8 * q + 3] = e4m3x2_to_half2(w.y >> 16);
+            r[8 * q + 4] = e4m3x2_to_half2(w.z);
+            r[8 * q + 5] = e4m3x2_to_half2(w.z >> 16);
+            r[8 * q + 6] = e4m3x2_to_half2(w.w);
+            r[8 * q + 7] = e4m3x2_to_half2(w.w >> 16);
+          }
+          tmem_st32(tmem + lane_q + C::kTAK + 64 * bb + 32 * h, r);
+        }
+      } else {
+        const uint4* kr = reinterpret_cast<const uint4*>(pg + L::kKey + off * 48);
+        const uint4 w0 = kr[0], w1 = kr[1], w2 = kr[2];
+        const uint32_t wd[12] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w, w2.x, w2.y, w2.z, w2.w};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r[32];
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int j = 32 * h + jj;  // coordinate pair j: codes of 2j, 2j+1 at bits 6j .. 6j+5
+            const int bit = 6 * j, wi = bit >> 5, sh = bit & 31;
+            uint32_t f = wd[wi] >> sh;
+            if (sh > 26) f |= wd[wi + 1] << (32 - sh);
+            r[jj] = pairs[(f & 63u) * 32 + lane];
+          }
+          tmem_st32(tmem + lane_q + C::kTAK + 64 * bb + 32 * h, r);
+        }
+      }
+      // ---- values of coordinate i -> A_V[bb], lane i, columns = token pairs
+      if (c >= 2 && !wait_bar(bars.pv(bb), ((c - 2) >> 1) & 1, abort_flag)) break;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[32];
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+          const int p = 4 * h + pp;
+          const uint2 w = *reinterpret_cast<const uint2*>(stage + p * L::kPage + L::kVal + 8 * i);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            r[8 * pp + k] = codebyte_to_half2((w.x >> (8 * k)) & 0xFFu);
+            r[8 * pp + 4 + k] = codebyte_to_half2((w.y >> (8 * k)) & 0xFFu);
+          }
+        }
+        tmem_st32(tmem + lane_q + C::kTAV + 64 * bb + 32 * h, r);
+      }
+      // ---- per-token parameters of token i for the softmax threads
+      {
+        const int pos = (page_lo + c * C::kPages) * kBlock + i;
+        const bool valid = pvalid[st * 8 + pg_i] != 0 && pos < t_hi;
+        float cs = sl2, sv = 0.f, zv = 0.f;
+        int rmin = 1 << 20;
+        if (valid) {
+          if constexpr (PRESET == 1)
+            cs = __half2float(*reinterpret_cast<const __half*>(pg + L::kNc + 2 * off)) * sl2;
+          sv = __half2float(*reinterpret_cast<const __half*>(pg + L::kScale + 2 * off));
+          zv = __half2float(*reinterpret_cast<const __half*>(pg + L::kZero + 2 * off));
+          rmin = 0;
+          if (a.causal) {
+            const int nmin = pos - L_b + a.n_spec;  // draft n sees this token iff n >= nmin
+            rmin = nmin <= 0 ? 0 : nmin * a.group;
+          }
+        }
+        colp[bb * 128 + i] = make_float4(cs, sv, zv, __int_as_float(rmin));
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bars.akv(bb));
+        mbar_arrive(bars.empty(st));
+      }
+    }
+  } else {
+    regs_inc<C::kRegSm>();
+    // ================= softmax: thread t = token t of the chunk, kNC query rows
+    const int t = tid - 256 - 128 * ((warp - 8) / 4);
+    const int wg = (warp - 8) / 4;  // softmax warpgroup: rows [wg * kNC, wg * kNC + kNC)
+    const int sw = warp & 3;
+    const uint32_t lane_q = (uint32_t)(sw * 32) << 16;
+    const uint32_t bar_id = 1 + wg;
+    float m[kNC], l[kNC], zs[kNC];
+#pragma unroll
+    for (int r = 0; r < kNC; ++r) {
+      m[r] = -CUDART_INF_F;
+      l[r] = 0.f;
+      zs[r] = 0.f;
+    }
+    bool aborted = false;
+    for (int c = 0; c < nchunks; ++c) {
+      const int bb = c & 1;
+      const bool ok = wait_bar(bars.qk(bb), (c >> 1) & 1, abort_flag) && wait_bar(bars.akv(bb), (c >> 1) & 1, abort_flag);
+      // leave the loop together: the named barriers below need all four warps
+      if (bar_red_or(bar_id, 128, !ok || aborted)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      const float4 cp = colp[bb * 128 + t];
+      const int rmin = __float_as_int(cp.w);
+      const uint32_t s_addr = tmem + lane_q + C::kTS + NMMA * bb + kNC * wg;
+      // scores of token t for this warpgroup's rows, scaled to log2 units, masked
+      float y[kNC];
+      auto load_scores = [&]() {
+        uint32_t r[kNC];
+        tmem_ld<kNC>(s_addr, r);
+        tc_wait_ld();
+#pragma unroll
+        for (int k = 0; k < kNC; ++k)
+          y[k] = (kNC * wg + k < rmin) ? -CUDART_INF_F : __uint_as_float(r[k]) * cp.x;
+      };
+      load_scores();
+      bool need = false;
+#pragma unroll
+      for (int k = 0; k < kNC; ++k) need |= y[k] > m[k] + kRescaleThreshold;
+      need = bar_red_or(bar_id, 128, need);
+      if (need) {
+        // exact maximum of this chunk for each row over the 128 tokens
+        // (reduces y in place; the scores are reloaded from tensor memory)
+        warp_transpose_reduce<kNC, true>(y, lane);
+        float* rmax = red + (wg * 3 + 0) * 4 * kNC;
+        if (lane < kNC) rmax[sw * kNC + lane] = y[0];
+        named_bar(bar_id, 128);
+        auto chunk_max = [&](int k) {
+          return fmaxf(fmaxf(rmax[k], rmax[kNC + k]), fmaxf(rmax[2 * kNC + k], rmax[3 * kNC + k]));
+        };
+        bool change = false;
+#pragma unroll
+        for (int k = 0; k < kNC; ++k) change |= chunk_max(k) > m[k];
+        const bool rescale_o = change && c > 0;  // uniform across the warpgroup
+        if (rescale_o) {
+          // O^T holds chunks < c: rescale it after the previous P.V has landed
+          // and before this chunk's is issued
+          if (!wait_bar(bars.pv((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag)) aborted = true;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int h = 0; h < kNC / 16; ++h) {
+          uint32_t r[16];
+          const uint32_t o_addr = tmem + lane_q + C::kTO + kNC * wg + 16 * h;
+          if (rescale_o) {
+            tmem_ld<16>(o_addr, r);
+            tc_wait_ld();
+          }
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int kk = 16 * h + k;
+            const float mn = fmaxf(m[kk], chunk_max(kk));
+            const float al = (mn == -CUDART_INF_F) ? 1.f : exp2f(m[kk] - mn);
+            m[kk] = mn;
+            l[kk] *= al;
+            zs[kk] *= al;
+            r[k] = __float_as_uint(__uint_as_float(r[k]) * al);
+          }
+          if (rescale_o) tmem_st<16>(o_addr, r);
+        }
+        if (rescale_o) tc_wait_st();
+        load_scores();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.sfree(bb));
+      if (c >= 2 && !wait_bar(bars.pv(bb), ((c - 2) >> 1) & 1, abort_flag)) aborted = true;
+      // probabilities, row sums, zero term; P' = p * scale into the MN-major B tile
+      uint8_t* pbuf = sm + C::kP + bb * C::kPBytes;
+#pragma unroll
+      for (int q = 0; q < kNC / 8; ++q) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k = 8 * q + 2 * e;
+          const float p0 = y[k] == -CUDART_INF_F ? 0.f : exp2f(y[k] - m[k]);
+          const float p1 = y[k + 1] == -CUDART_INF_F ? 0.f : exp2f(y[k + 1] - m[k + 1]);
+          l[k] += p0;
+          l[k + 1] += p1;
+          zs[k] = fmaf(p0, cp.z, zs[k]);
+          zs[k + 1] = fmaf(p1, cp.z, zs[k + 1]);
+          pk[e] = pack_half2(p0 * cp.y, p1 * cp.y);
+        }
+        const uint32_t lg = (uint32_t)((t >> 3) * (8 * C::kLine) + (t & 7) * C::kLine + wg * kNC * 2 + 16 * q);
+        const uint32_t ph = lg ^ (((lg >> 7) & ((1u << C::kSwzBits) - 1u)) << 4);
+        *reinterpret_cast<uint4*>(pbuf + ph) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.pfull(bb));
+    }
+    // ---- epilogue: l and zero term over all 128 tokens, then O^T / l
+    {
+      float v[kNC];
+#pragma unroll
+      for (int k = 0; k < kNC; ++k) v[k] = l[k];
+      warp_transpose_reduce<kNC, false>(v, lane);
+      float* rl = red + (wg * 3 + 1) * 4 * kNC;
+      if (lane < kNC) rl[sw * kNC + lane] = v[0];
+#pragma unroll
+      for (int k = 0; k < kNC; ++k) v[k] = zs[k];
+      warp_transpose_reduce<kNC, false>(v, lane);
+      float* rz = red + (wg * 3 + 2) * 4 * kNC;
+      if (lane < kNC) rz[sw * kNC + lane] = v[0];
+    }
+    named_bar(bar_id, 128);
+    uint32_t o[kNC];
+#pragma unroll
+    for (int k = 0; k < kNC; ++k) o[k] = 0u;
+    if (nchunks > 0 && !aborted) {
+      const int lc = nchunks - 1;
+      if (wait_bar(bars.pv(lc & 1), (lc >> 1) & 1, abort_flag)) {
+        tc_fence_after();
+        tmem_ld<kNC>(tmem + lane_q + C::kTO + kNC * wg, o);
+        tc_wait_ld();
+      } else {
+        aborted = true;
+      }
+    }
+    aborted = aborted || (*abort_flag != 0u);
+    const float* rl = red + (wg * 3 + 1) * 4 * kNC;
+    const float* rz = red + (wg * 3 + 2) * 4 * kNC;
+#pragma unroll
+    for (int k = 0; k < kNC; ++k) {
+      const int row = kNC * wg + k;
+      if (row < a.R) {
+        const float lt = (rl[k] + rl[kNC + k]) + (rl[2 * kNC + k] + rl[3 * kNC + k]);
+        const float zt = (rz[k] + rz[kNC + k]) + (rz[2 * kNC + k] + rz[3 * kNC + k]);
+        const int n = row / a.group, jj = row % a.group;
+        const long orow = (((long)n * a.B + b) * a.Hq + kvh * a.group + jj) * a.S + split;
+        float val = lt > 0.f ? (__uint_as_float(o[k]) + zt) / lt : 0.f;
+        if (aborted) val = CUDART_NAN_F;
+        a.part_o[orow * kD + t] = val;
+        if (t == 0) a.part_lse[orow] = aborted ? CUDART_NAN_F : (lt > 0.f ? (m[k] + log2f(lt)) * kLn2 : -CUDART_INF_F);
+      }
+    }
+  }
+
+  // ---- teardown: every role has drained its asynchronous work
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int PRESET, int NMMA>
+cudaError_t launch_tc(const VerifyArgs& a, cudaStream_t st) {
+  using C = Cfg<PRESET, NMMA>;
+  auto kern = verify_stage1_tc_kernel<PRESET, NMMA>;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    // setmaxnreg.inc waits for registers released by other warps of the CTA:
+    // refuse to launch if the compiled register count cannot cover the split
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs * C::kThreads < C::kRegNeeded) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  dim3 grid(a.S, a.Hk, a.B);
+  kern<<<grid, C::kThreads, C::kSmem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool verify_stage1_tc_supported(const VerifyArgs& a) { return a.R <= 64; }
+
+cudaError_t launch_verify_stage1_tc(int preset, const VerifyArgs& a, cudaStream_t st) {
+  if (preset == 0) {
+    if (a.R <= 16) return launch_tc<0, 16>(a, st);
+    if (a.R <= 32) return launch_tc<0, 32>(a, st);
+    return launch_tc<0, 64>(a, st);
+  }
+  if (a.R <= 16) return launch_tc<1, 16>(a, st);
+  if (a.R <= 32) return launch_tc<1, 32>(a, st);
+  return launch_tc<1, 64>(a, st);
+}
+
+cudaError_t read_device_error(unsigned int* out, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_tq_device_error, sizeof(unsigned int));
+  if (e != cudaSuccess || !clear) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_tq_device_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace tq

@@ -75,6 +75,8 @@ def load(build_if_missing: bool = False):
         lib.tq_verify_stage1.argtypes = [D, P, P, I, P, I, I, I, I, I, P, P, P]
         lib.tq_verify_stage2.restype = I
         lib.tq_verify_stage2.argtypes = [P, P, I, I, I, I, I, P, P]
+        lib.tq_device_status.restype = I
+        lib.tq_device_status.argtypes = []
         _lib = lib
         return lib
 
@@ -116,6 +118,11 @@ def tq_codebook(preset: int = TQ_PRESET_K3V4_NC) -> np.ndarray:
     out = np.zeros(8, np.float32)
     _check(load().tq_codebook(int(preset), ctypes.c_void_p(out.ctypes.data)), "tq_codebook")
     return out
+
+
+def tq_device_status() -> int:
+    """Reads and clears the sticky device-side error word (synchronises)."""
+    return int(load().tq_device_status())
 
 
 def tq_status_string(status: int) -> str:

@@ -28,7 +28,7 @@ def declared_functions():
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert {"tq_store", "tq_verify_stage1", "tq_verify_stage2", "tq_page_bytes",
-            "tq_partials_bytes", "tq_codebook", "tq_status_string"} <= set(names)
+            "tq_partials_bytes", "tq_codebook", "tq_status_string", "tq_device_status"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
 

@@ -37,6 +37,9 @@ SMALL = [
     ("k3v4_nc", 4, 2, 6, 3, 40, 1, True),
     ("k8v4", 3, 2, 2, 2, 3, 4, True),       # cached_len 0, splits mostly empty
     ("k3v4_nc", 8, 1, 32, 4, 555, 7, True),
+    ("k8v4", 4, 2, 8, 1, 300, 3, True),     # 32 rows per kv-head
+    ("k3v4_nc", 2, 1, 16, 1, 77, 2, True),
+    ("k3v4_nc", 16, 1, 16, 2, 190, 3, True),  # 128 rows per kv-head
 ]
 
 
@@ -209,6 +212,12 @@ def test_invalid_block_ids_are_invisible(oracle_lib):
     assert_close(sv.out.cpu().numpy(), ref)
 
 
+def test_device_status_clean():
+    """No bounded device-side wait expired in any of the runs above."""
+    torch.cuda.synchronize()
+    assert tqkv.tq_device_status() == tqkv.TQ_OK
+
+
 def test_unused_slots_with_garbage_do_not_leak():
     """Slots past seq_len in the last page hold arbitrary bytes (here 0xFF:
     NaN scales); the output must not change."""
@@ -222,11 +231,13 @@ def test_unused_slots_with_garbage_do_not_leak():
     ref = sv.verify().clone()
     last = int(inp.block_table[0, (200 - 1) // 16])
     page = sv.caches[0][last, 0]
-    for off in range(200 % 16, 16):
+    assert 200 % 16 == 8  # tokens 8..15 of the last page are unused
+    for off in range(8, 16):
         page[off * 128:(off + 1) * 128] = 0xFF            # NaN e4m3 keys
-        page[2048 + off * 64: 2048 + off * 64 + 64] = 0xFF
         page[3072 + 2 * off: 3072 + 2 * off + 2] = 0xFF   # NaN scale
         page[3104 + 2 * off: 3104 + 2 * off + 2] = 0xFF   # NaN zero
+    for d in range(128):                                   # value codes of tokens 8..15:
+        page[2048 + 8 * d + 4: 2048 + 8 * d + 8] = 0xFF    # bytes 4..7 of each coordinate row
     out = sv.verify()
     torch.cuda.synchronize()
     assert torch.equal(out, ref)

@@ -152,12 +152,10 @@ def test_key8_is_per_coordinate_e4m3(oracle_lib):
 
 # ------------------------------------------------------------------ values
 
-def _decode_v(packed, s, z):
+def _decode_v(codes, s, z):
     sf = np.float64(np.array([s], np.uint16).view(np.float16)[0])
     zf = np.float64(np.array([z], np.uint16).view(np.float16)[0])
-    codes = np.empty(D, np.int64)
-    codes[0::2] = packed & 15
-    codes[1::2] = packed >> 4
+    codes = codes.astype(np.int64)
     return codes, codes * sf + zf, sf, zf
 
 
@@ -207,10 +205,10 @@ def test_page_layout_and_skips(oracle_lib, preset, offs):
     nb, hk = 3, 2
     assert O.page_bytes(preset) == offs["page"]
     cache = np.zeros((nb, hk, offs["page"]), np.uint8)
-    T = 5
+    T = 7
     k = rng.standard_normal((T, hk, D)).astype(np.float16)
     v = rng.standard_normal((T, hk, D)).astype(np.float16)
-    slots = np.array([17, -1, 3, nb * 16, 40], np.int32)
+    slots = np.array([17, -1, 3, nb * 16, 40, 16, 2], np.int32)  # 16/17 and 2/3 share value bytes
     O.store(preset, cache, k, v, slots)
     expect = np.zeros_like(cache)
     for t, slot in enumerate(slots):
@@ -226,7 +224,11 @@ def test_page_layout_and_skips(oracle_lib, preset, offs):
                 codes, nc = O.encode_key3(k[t, h])
                 pg[off * 48:(off + 1) * 48] = codes
                 pg[offs["nc"] + 2 * off: offs["nc"] + 2 * off + 2] = np.array([nc], "<u2").view(np.uint8)
-            pg[offs["v"] + off * 64: offs["v"] + off * 64 + 64] = vp
+            # value codes coordinate-major: byte 8d + off/2, low nibble = even off
+            for d in range(D):
+                byte = offs["v"] + 8 * d + off // 2
+                sh = 4 * (off % 2)
+                pg[byte] = (int(pg[byte]) & (0xFF ^ (0xF << sh))) | (int(vp[d]) << sh)
             pg[offs["s"] + 2 * off: offs["s"] + 2 * off + 2] = np.array([s], "<u2").view(np.uint8)
             pg[offs["z"] + 2 * off: offs["z"] + 2 * off + 2] = np.array([z], "<u2").view(np.uint8)
     assert np.array_equal(cache, expect)
