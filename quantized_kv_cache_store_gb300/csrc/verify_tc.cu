@@ -100,9 +100,9 @@ struct Cfg {
   static constexpr int kQBytes = 2 * NMMA * 128;  // K-major, 128B swizzle, 2 x 64-coordinate blocks
   static constexpr int kP = kQ + align_up(kQBytes, 1024);
   static constexpr int kPBytes = kTok * kLine;  // one buffer
-  static constexpr int kCol = kP + 2 * kPBytes;  // float4 [2][128]: column scale, v scale, v zero, row mask
-  static constexpr int kRed = kCol + 2 * kTok * 16;  // float [kW][3][4][16]
-  static constexpr int kPair = kRed + kW * 3 * 4 * kNC * 4;  // u32 [64][32] (k3v4_nc)
+  static constexpr int kCol = kP + 2 * kPBytes;  // float4 [3][128]: column scale, v scale, v zero, row mask
+  static constexpr int kRed = kCol + 3 * kTok * 16;  // float [kW][3][4][16], then float [kW][3][16]
+  static constexpr int kPair = kRed + kW * 3 * 5 * kNC * 4;  // u32 [64][32] (k3v4_nc)
   static constexpr int kPValid = kPair + (PRESET == 1 ? 64 * 32 * 4 : 0);  // u8 [kStages][8]
   static constexpr int kBar = align_up(kPValid + kStages * 8, 8);
   // full[kStages] empty[kStages] akv[2] qk[2] sfree[2] pfull[2] pv[2]
@@ -432,10 +432,13 @@ __global__ void __launch_bounds__(Cfg<PRESET, NMMA>::kThreads, 1)
     const uint32_t lane_q = (uint32_t)(sw * 32) << 16;
     const uint32_t bar_id = 1 + wg;
     const int pg_t = t >> 4, off_t = t & 15;  // token t of a chunk: page and row
+    // running maxima start at a finite floor: a masked score (-inf) then always
+    // gives p = 2^-inf = 0, and the first visible score forces a rescale
+    constexpr float kFloor = -1.0e30f;
     float m[kNC], l[kNC], zs[kNC];
 #pragma unroll
     for (int r = 0; r < kNC; ++r) {
-      m[r] = -CUDART_INF_F;
+      m[r] = kFloor;
       l[r] = 0.f;
       zs[r] = 0.f;
     }
@@ -445,10 +448,10 @@ __global__ void __launch_bounds__(Cfg<PRESET, NMMA>::kThreads, 1)
       if (it < nchunks && !aborted) {
         const int c = it, st = c % C::kStages, bb = c & 1;
         bool ok = wait_bar(bars.full(st), (c / C::kStages) & 1, abort_flag);
-        if (ok && c >= 2) {
-          ok = wait_bar(bars.qk(bb), ((c - 2) >> 1) & 1, abort_flag);  // A_K[c % 2] read by S^T(c - 2)
-          if (ok && wg == 0) ok = wait_bar(bars.sfree(bb), ((c - 2) >> 1) & 1, abort_flag);  // token params
-        }
+        if (ok && c >= 2) ok = wait_bar(bars.qk(bb), ((c - 2) >> 1) & 1, abort_flag);  // A_K[c % 2] read by S^T(c - 2)
+        // token params [c % 3] read by softmax(c - 3) before its sfree; softmax(c - 1)
+        // on the same barrier cannot finish before this warpgroup's part B of it
+        if (ok && c >= 3 && wg == 0) ok = wait_bar(bars.sfree((c - 3) & 1), ((c - 3) >> 1) & 1, abort_flag);
         // A_V[c % 3] read by O^T(c - 3); O^T(c - 1), on the same barrier, is not
         // issued before every worker has finished this part, so the parity is unambiguous
         if (ok && c >= 3) ok = wait_bar(bars.pv((c - 3) & 1), ((c - 3) >> 1) & 1, abort_flag);
@@ -536,7 +539,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NMMA>::kThreads, 1)
                 rmin = nmin <= 0 ? 0 : nmin * a.group;
               }
             }
-            colp[bb * 128 + t] = make_float4(cs, sv, zv, __int_as_float(rmin));
+            colp[(c % 3) * 128 + t] = make_float4(cs, sv, zv, __int_as_float(rmin));
           }
           tc_wait_st();
           tc_fence_before();
@@ -558,7 +561,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NMMA>::kThreads, 1)
           break;
         }
         tc_fence_after();
-        const float4 cp = colp[bb * 128 + t];
+        const float4 cp = colp[(c % 3) * 128 + t];
         const int rmin = __float_as_int(cp.w);
         const uint32_t s_addr = tmem + lane_q + C::kTS + NMMA * bb + kNC * wg;
         float y[kNC];
@@ -566,9 +569,14 @@ __global__ void __launch_bounds__(Cfg<PRESET, NMMA>::kThreads, 1)
           uint32_t r[kNC];
           tmem_ld<kNC>(s_addr, r);
           tc_wait_ld();
+          if (__all_sync(kFull, rmin <= kNC * wg)) {  // every row of this warpgroup sees these tokens
 #pragma unroll
-          for (int k = 0; k < kNC; ++k)
-            y[k] = (kNC * wg + k < rmin) ? -CUDART_INF_F : __uint_as_float(r[k]) * cp.x;
+            for (int k = 0; k < kNC; ++k) y[k] = __uint_as_float(r[k]) * cp.x;
+          } else {
+#pragma unroll
+            for (int k = 0; k < kNC; ++k)
+              y[k] = (kNC * wg + k < rmin) ? -CUDART_INF_F : __uint_as_float(r[k]) * cp.x;
+          }
         };
         load_scores();
         bool need = false;
@@ -604,7 +612,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NMMA>::kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kNC; ++k) {
             const float mn = fmaxf(m[k], y[k]);
-            const float al = (mn == -CUDART_INF_F) ? 1.f : ex2(m[k] - mn);
+            const float al = ex2(m[k] - mn);
             m[k] = mn;
             l[k] *= al;
             zs[k] *= al;
@@ -628,8 +636,8 @@ __global__ void __launch_bounds__(Cfg<PRESET, NMMA>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int k = 8 * q + 2 * e;
-            const float p0 = y[k] == -CUDART_INF_F ? 0.f : ex2(y[k] - m[k]);
-            const float p1 = y[k + 1] == -CUDART_INF_F ? 0.f : ex2(y[k + 1] - m[k + 1]);
+            const float p0 = ex2(y[k] - m[k]);
+            const float p1 = ex2(y[k + 1] - m[k + 1]);
             l[k] += p0;
             l[k + 1] += p1;
             zs[k] = fmaf(p0, cp.z, zs[k]);
@@ -675,21 +683,37 @@ __global__ void __launch_bounds__(Cfg<PRESET, NMMA>::kThreads, 1)
       }
     }
     aborted = aborted || (*abort_flag != 0u);
-    const float* rl = red + (wg * 3 + 1) * 4 * kNC;
-    const float* rz = red + (wg * 3 + 2) * 4 * kNC;
+    // per-row constants (threads 0..15): 1 / l, zero term / l, log-sum-exp
+    float* rowc = red + C::kW * 3 * 4 * kNC + wg * 2 * kNC;
+    if (t < kNC) {
+      const float* rl = red + (wg * 3 + 1) * 4 * kNC;
+      const float* rz = red + (wg * 3 + 2) * 4 * kNC;
+      const float lt = (rl[t] + rl[kNC + t]) + (rl[2 * kNC + t] + rl[3 * kNC + t]);
+      const float zt = (rz[t] + rz[kNC + t]) + (rz[2 * kNC + t] + rz[3 * kNC + t]);
+      float mt = m[0];
+#pragma unroll
+      for (int k = 1; k < kNC; ++k) mt = (t == k) ? m[k] : mt;
+      const float inv = lt > 0.f ? 1.0f / lt : 0.f;
+      rowc[t] = inv * 16777216.0f;  // O^T holds the value codes as fp16 subnormals (code * 2^-24)
+      rowc[kNC + t] = zt * inv;
+      const int row = kNC * wg + t;
+      if (row < a.R) {
+        const long orow = (((long)(row / a.group) * a.B + b) * a.Hq + kvh * a.group + row % a.group) * a.S + split;
+        a.part_lse[orow] = aborted ? CUDART_NAN_F : (lt > 0.f ? (mt + log2f(lt)) * kLn2 : -CUDART_INF_F);
+      }
+    }
+    named_bar(bar_id, 128);
+    // rows 16 wg + k = n * group + j, walked incrementally
+    int jj = (kNC * wg) % a.group;
+    float* po = a.part_o + ((((long)((kNC * wg) / a.group) * a.B + b) * a.Hq + kvh * a.group + jj) * a.S + split) * kD + t;
+    const long step_j = (long)a.S * kD, step_n = ((long)a.B * a.Hq - a.group) * a.S * kD;
 #pragma unroll
     for (int k = 0; k < kNC; ++k) {
-      const int row = kNC * wg + k;
-      if (row < a.R) {
-        const float lt = (rl[k] + rl[kNC + k]) + (rl[2 * kNC + k] + rl[3 * kNC + k]);
-        const float zt = (rz[k] + rz[kNC + k]) + (rz[2 * kNC + k] + rz[3 * kNC + k]);
-        const int n = row / a.group, jj = row % a.group;
-        const long orow = (((long)n * a.B + b) * a.Hq + kvh * a.group + jj) * a.S + split;
-        // O^T accumulated the value codes as fp16 subnormals (code * 2^-24)
-        float val = lt > 0.f ? (__uint_as_float(o[k]) * 16777216.0f + zt) / lt : 0.f;
-        if (aborted) val = CUDART_NAN_F;
-        a.part_o[orow * kD + t] = val;
-        if (t == 0) a.part_lse[orow] = aborted ? CUDART_NAN_F : (lt > 0.f ? (m[k] + log2f(lt)) * kLn2 : -CUDART_INF_F);
+      if (kNC * wg + k < a.R) *po = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rowc[k], rowc[kNC + k]);
+      po += step_j;
+      if (++jj == a.group) {
+        jj = 0;
+        po += step_n;
       }
     }
   }
