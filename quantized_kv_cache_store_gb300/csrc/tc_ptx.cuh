@@ -38,6 +38,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uin
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 
 // ------------------------------------------------ bulk copy (non-tensor TMA)
 // dst, src 16-byte aligned, bytes a multiple of 16; completes tx on `bar`.
@@ -60,14 +70,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int 
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
+// Named barriers in their non-aligned form: a warp may arrive diverged (for
+// example after a lane-0-only branch); every thread is counted on arrival.
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t n) {
-  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+  asm volatile("barrier.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
 }
+// all threads of the CTA (barrier 0)
+__device__ __forceinline__ void cta_bar() { asm volatile("barrier.sync 0;\n" ::: "memory"); }
 // barrier over n threads with an OR-reduction of `pred`
 __device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t n, bool pred) {
   uint32_t out;
   asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(out)
       : "r"((uint32_t)pred), "r"(id), "r"(n)
       : "memory");
@@ -101,6 +115,32 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t bdesc, u
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
       "r"(a), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+// Eight MMAs D (+)= A_k * B_k, k = 0..7, into the same accumulator, issued
+// back to back: A_k at tensor-memory column a + 8 k, B_k's descriptor =
+// bdesc + boff[k] (start-address units of 16 bytes).  The first MMA
+// accumulates iff acc0; the others always do.
+template <uint32_t O1, uint32_t O2, uint32_t O3, uint32_t O4, uint32_t O5, uint32_t O6, uint32_t O7>
+__device__ __forceinline__ void mma_ts_x8(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n .reg .pred p, t;\n .reg .b64 b1, b2, b3, b4, b5, b6, b7;\n .reg .b32 a1, a2, a3, a4, a5, a6, a7;\n"
+      " setp.ne.b32 p, %4, 0;\n setp.eq.b32 t, %4, %4;\n"
+      " add.u64 b1, %2, %5;\n add.u64 b2, %2, %6;\n add.u64 b3, %2, %7;\n add.u64 b4, %2, %8;\n"
+      " add.u64 b5, %2, %9;\n add.u64 b6, %2, %10;\n add.u64 b7, %2, %11;\n"
+      " add.u32 a1, %1, 8;\n add.u32 a2, %1, 16;\n add.u32 a3, %1, 24;\n add.u32 a4, %1, 32;\n"
+      " add.u32 a5, %1, 40;\n add.u32 a6, %1, 48;\n add.u32 a7, %1, 56;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %3, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %3, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %3, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %3, t;\n}\n" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(idesc), "r"(acc0), "n"((uint64_t)O1), "n"((uint64_t)O2), "n"((uint64_t)O3),
+      "n"((uint64_t)O4), "n"((uint64_t)O5), "n"((uint64_t)O6), "n"((uint64_t)O7)
       : "memory");
 }
 

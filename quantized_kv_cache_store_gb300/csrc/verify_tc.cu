@@ -13,18 +13,22 @@
 // transposed so that the 128-row side of the MMA is tokens or coordinates:
 //   S^T[token, row]  = K_hat[token, :] . Q[row, :]         (M = 128, N = rows)
 //   O^T[d, row]     += V_codes^T[d, token] . P'[row, token] (M = 128, N = rows)
-// with A operands in tensor memory (written by the worker threads with
-// tcgen05.st) and B operands in shared memory (Q once per CTA; P' per chunk).
+// with A operands in tensor memory (written with tcgen05.st) and B operands
+// in shared memory (Q once per CTA; P' per chunk).
 //   keys   : k8v4 e4m3 -> f16 exactly (the key block of a page arrives by TMA
 //            with 128-byte swizzle, so the per-token row reads are free of
 //            bank conflicts); k3v4_nc 3-bit code pairs -> fp16 centroid pairs
 //            through a per-lane replicated table; the norm correction nc_t
-//            scales token t's scores (its TMEM lane) after the MMA; the query
-//            is rotated once, q_rot = H q / sqrt(D).
-//   values : codes enter as exact fp16 subnormals (code * 2^-24, undone on
-//            the output); P' = p * scale_t; the zero term sum_t p_t zero_t and
-//            l = sum_t p_t are kept per thread in fp32, reduced at the end.
-// Softmax: thread t owns token t (its S^T lane) and 16 query rows.  The
+//            scales token t's scores after the MMA; the query is rotated
+//            once, q_rot = H q / sqrt(D).
+//   values : a 4-bit code c enters the MMA as the fp16 subnormal c * 2^-24
+//            (even tokens) or 16 c * 2^-24 (odd tokens, whose probability is
+//            divided by 16), so that one 32-bit word of eight codes becomes
+//            four f16x2 operand words with one shift and four masks; the
+//            factor 2^24 is undone on the output.  P' = p * scale_t; the zero
+//            term sum_t p_t zero_t and l = sum_t p_t are kept per thread in
+//            fp32 and reduced at the end.
+// Softmax: thread t owns token t (its S^T lane) and up to 32 query rows.  The
 // running maximum is updated lazily: only when some score exceeds it by more
 // than 8 (log2 units) is the exact chunk maximum computed across the 128
 // tokens and O^T, l and the zero term rescaled; otherwise probabilities stay
@@ -32,14 +36,12 @@
 // same softmax).
 //
 // Warp roles: warp 0 = producer (block ids + copies), warp 1 = MMA issuer,
-// warp 2 = TMEM owner.  Worker warpgroup j (NMMA / 16 of them) dequantises its
-// share of chunk c (A_K columns and A_V columns [64/W j, 64/W (j+1)); A_V is
-// triple-buffered so that chunk c does not wait for O^T(c - 1)) and then
-// runs the softmax of chunk c - 1 for query rows [16 j, 16 j + 16), so every
-// scheduler keeps several warps busy.  Every wait on an mbarrier is bounded:
-// on expiry the CTA sets an abort flag and the sticky device error word,
-// drains its in-flight copies and MMAs, frees its tensor memory and writes
-// NaN partials.
+// warp 2 = TMEM owner; warpgroup 1 dequantises chunk c (A_K[c % 2], A_V[c % 3]
+// and the per-token parameters) while softmax warpgroup j (rows [32 j,
+// 32 j + 32)) works on an earlier chunk.  Every wait on an mbarrier is
+// bounded: on expiry the CTA sets an abort flag and the sticky device error
+// word, drains its in-flight copies and MMAs, frees its tensor memory and
+// writes NaN partials.
 #include <math_constants.h>
 
 #include <atomic>
@@ -47,7 +49,6 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
-#include <cuda_fp8.h>
 
 #include "tc_ptx.cuh"
 #include "tq_common.cuh"
@@ -70,7 +71,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between resca
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-template <int PRESET, int NMMA>
+template <int PRESET, int NR>
 struct Cfg {
   using L = Layout<PRESET>;
   static constexpr int kTok = 128;  // tokens per chunk
@@ -82,53 +83,57 @@ struct Cfg {
   static constexpr int kRestOff = kPages * kKeyBlock;
   static constexpr int kStageBytes = align_up(kPages * L::kPage, 1024);
   static constexpr int kStages = PRESET == 0 ? 4 : 6;
-  static constexpr int kW = NMMA / 16;   // worker warpgroups
-  static constexpr int kNC = 16;         // query rows per worker thread
-  static constexpr int kKC = 64 / kW;    // A-operand columns each worker warpgroup writes
-  static constexpr int kThreads = 128 + 128 * kW;
-  // per-thread register budgets after setmaxnreg (control / workers); their
-  // sum must stay within what the launch granted (checked at launch)
-  static constexpr int kRegCtl = 32;
-  static constexpr int kRegW = kW == 4 ? 112 : (kW == 2 ? 200 : 232);
-  static constexpr int kRegNeeded = 128 * kRegCtl + 128 * kW * kRegW;
-  static constexpr int kLine = 2 * NMMA;  // bytes of one P' line (one token)
-  static constexpr int kSwzBits = NMMA == 64 ? 3 : (NMMA == 32 ? 2 : 1);
-  static constexpr uint32_t kSwzMode = NMMA == 64 ? 2u : (NMMA == 32 ? 4u : 6u);
+  static constexpr int kSW = NR == 64 ? 2 : 1;    // softmax warpgroups
+  static constexpr int kRS = NR == 64 ? 32 : NR;  // query rows per softmax thread
+  static constexpr int kThreads = 256 + 128 * kSW;
+  // per-thread register budgets after setmaxnreg (control / dequant /
+  // softmax); their sum must stay within what the launch granted (checked at
+  // launch: 128 registers a thread for 512 threads, 168 for 384)
+  static constexpr int kRegCtl = kSW == 2 ? 40 : 32;
+  static constexpr int kRegDq = 96;
+  static constexpr int kRegSm = kSW == 2 ? 184 : 232;
+  static constexpr int kRegNeeded = 128 * kRegCtl + 128 * kRegDq + 128 * kSW * kRegSm;
+  static constexpr int kLine = 2 * NR;  // bytes of one P' line (one token)
+  static constexpr int kSwzBits = NR == 64 ? 3 : (NR == 32 ? 2 : 1);
+  static constexpr uint32_t kSwzMode = NR == 64 ? 2u : (NR == 32 ? 4u : 6u);
   // shared memory (offsets from a 1024-byte aligned base)
   static constexpr int kRing = 0;
   static constexpr int kQ = align_up(kStages * kStageBytes, 1024);
-  static constexpr int kQBytes = 2 * NMMA * 128;  // K-major, 128B swizzle, 2 x 64-coordinate blocks
+  static constexpr int kQBytes = 2 * NR * 128;  // K-major, 128B swizzle, 2 x 64-coordinate blocks
   static constexpr int kP = kQ + align_up(kQBytes, 1024);
   static constexpr int kPBytes = kTok * kLine;  // one buffer
-  static constexpr int kCol = kP + 2 * kPBytes;  // float4 [3][128]: column scale, v scale, v zero, row mask
-  static constexpr int kRed = kCol + 3 * kTok * 16;  // float [kW][3][4][16], then float [kW][3][16]
-  static constexpr int kPair = kRed + kW * 3 * 5 * kNC * 4;  // u32 [64][32] (k3v4_nc)
+  static constexpr int kCol = kP + 3 * kPBytes;  // float4 [3][128]: score scale, P' scale, v zero, first row
+  static constexpr int kRed = kCol + 3 * kTok * 16;  // per softmax warpgroup: float [3][4][32] + [2][32] + [32]
+  static constexpr int kRedWG = (3 * 4 * 32 + 2 * 32 + 32) * 4;
+  static constexpr int kPair = kRed + kSW * kRedWG;  // u32 [64][32] (k3v4_nc)
   static constexpr int kPValid = kPair + (PRESET == 1 ? 64 * 32 * 4 : 0);  // u8 [kStages][8]
   static constexpr int kBar = align_up(kPValid + kStages * 8, 8);
-  // full[kStages] empty[kStages] akv[2] qk[2] sfree[2] pfull[2] pv[2]
-  static constexpr int kNumBars = 2 * kStages + 10;
+  // full[kStages] empty[kStages] akv[3] qk[2] pfull[3] pv[3]
+  static constexpr int kNumBars = 2 * kStages + 11;
   static constexpr int kMisc = kBar + 8 * kNumBars;  // u32 tmem base, u32 abort
   static constexpr int kSmem = kMisc + 16 + 1024;    // + alignment slack
   // tensor memory columns
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kTAK = 0;     // A_K[2]: 64 cols each (token lanes, coordinate pairs)
-  static constexpr uint32_t kTAV = 128;   // A_V[3]: 64 cols each (coordinate lanes, token pairs)
-  static constexpr uint32_t kTS = 320;    // S^T[2]: NMMA cols each
-  static constexpr uint32_t kTO = 320 + 2 * NMMA;  // O^T: NMMA cols
-  static_assert(kTO + NMMA <= kTmemCols, "tensor memory overflow");
+  static constexpr uint32_t kTAK = 0;    // A_K[2]: 64 cols each (token lanes, coordinate pairs)
+  static constexpr uint32_t kTAV = 128;  // A_V[3]: 64 cols each (coordinate lanes, token pairs)
+  static constexpr uint32_t kTS = 320;   // S^T[2]: NR cols each
+  static constexpr uint32_t kTO = 320 + 2 * NR;  // O^T: NR cols
+  static_assert(kTO + NR <= kTmemCols, "tensor memory overflow");
   static_assert(kSmem <= 227 * 1024, "shared memory overflow");
 };
 
+// Barriers.  Rings indexed by c % 3 (akv, pv) are one deeper than the
+// distance at which they are reused, so that a waiter never sees a barrier
+// two phases ahead of the one it waits for.
 struct Bars {
   uint32_t base;
   int stages;
   __device__ uint32_t full(int s) const { return base + 8 * s; }
   __device__ uint32_t empty(int s) const { return base + 8 * (stages + s); }
-  __device__ uint32_t akv(int b) const { return base + 8 * (2 * stages + b); }        // A operands + token params
-  __device__ uint32_t qk(int b) const { return base + 8 * (2 * stages + 2 + b); }     // S^T = K Q^T done
-  __device__ uint32_t sfree(int b) const { return base + 8 * (2 * stages + 4 + b); }  // S^T read by softmax
-  __device__ uint32_t pfull(int b) const { return base + 8 * (2 * stages + 6 + b); }  // P' written
-  __device__ uint32_t pv(int b) const { return base + 8 * (2 * stages + 8 + b); }     // O^T += V^T P'^T done
+  __device__ uint32_t akv(int i) const { return base + 8 * (2 * stages + i); }        // A operands + token params (c % 3)
+  __device__ uint32_t qk(int b) const { return base + 8 * (2 * stages + 3 + b); }     // S^T = K Q^T done (c % 2)
+  __device__ uint32_t pfull(int i) const { return base + 8 * (2 * stages + 5 + i); }  // P' written, S^T read (c % 3)
+  __device__ uint32_t pv(int i) const { return base + 8 * (2 * stages + 8 + i); }     // O^T += V^T P'^T done (c % 3)
 };
 
 // Bounded wait; false when the CTA aborted or this wait expired (which aborts).
@@ -145,9 +150,12 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
-__device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t w16) {
-  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w16 & 0xFFFFu), __NV_E4M3);
-  return (uint32_t)r.x | ((uint32_t)r.y << 16);
+// two e4m3 codes (low and high byte) -> two f16 (exact)
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w16) {
+  uint32_t r;
+  const uint16_t h = (uint16_t)(w16 & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
+  return r;
 }
 
 // 2^x, hardware approximation (relative error ~2^-22), -inf -> 0
@@ -155,6 +163,12 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -186,34 +200,26 @@ __device__ __forceinline__ void warp_transpose_reduce(float (&v)[NC], int lane) 
   }
 }
 
-template <int N>
-__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
-  if constexpr (N == 16) {
-    tmem_st<16>(taddr, r);
-  } else {
-#pragma unroll
-    for (int h = 0; h < N / 32; ++h) {
-      uint32_t q[32];
-#pragma unroll
-      for (int k = 0; k < 32; ++k) q[k] = r[32 * h + k];
-      tmem_st<32>(taddr + 32 * h, q);
-    }
-  }
+// Position of chunk token t on the K axis of the P.V contraction.  Within
+// each group of 8 tokens the value operand holds the pairs (0,5) (1,4) (2,7)
+// (3,6), the order the nibble masks produce.
+__device__ __forceinline__ int kappa(int t) {
+  constexpr uint32_t kPos = 0x57136420u;  // nibble k: position of token k of a group
+  return (t & ~7) | (int)((kPos >> (4 * (t & 7))) & 7u);
 }
 
-template <int PRESET, int NMMA>
-__global__ void __launch_bounds__(Cfg<PRESET, NMMA>::kThreads, 1)
+template <int PRESET, int NR>
+__global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     verify_stage1_tc_kernel(VerifyArgs a, const __grid_constant__ CUtensorMap tmap_keys) {
-  using C = Cfg<PRESET, NMMA>;
+  using C = Cfg<PRESET, NR>;
   using L = typename C::L;
-  constexpr int kNC = C::kNC, kKC = C::kKC;
+  constexpr int kRS = C::kRS;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(sm);
   uint8_t* pvalid = sm + C::kPValid;
   float4* colp = reinterpret_cast<float4*>(sm + C::kCol);
-  float* red = reinterpret_cast<float*>(sm + C::kRed);
   uint32_t* pairs = reinterpret_cast<uint32_t*>(sm + C::kPair);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sm + C::kMisc + 4);
@@ -234,19 +240,58 @@ __global__ void __launch_bounds__(Cfg<PRESET, NMMA>::kThreads, 1)
   const int nchunks = (npages + C::kPages - 1) / C::kPages;
   const int32_t* bt = a.block_table + (long)b * a.max_blocks;
 
+  // Producer = warp 0 (all lanes wait together; lane 0 issues the copies).
+  // Block ids are fetched 32 pages (4 chunks) at a time, one id per lane.
+  int ids = -1;  // this lane's block id for page 32 * (c / 4) + lane
+  auto fetch_ids = [&](int c) {
+    const int lp = c * C::kPages + lane;
+    ids = -1;
+    if (lp < npages) {
+      const int id = bt[page_lo + lp];
+      ids = (id >= 0 && id < a.num_blocks) ? id : -1;
+    }
+  };
+  auto produce = [&](int c) {
+    const int st = c % C::kStages;
+    const int mine = __shfl_sync(kFull, ids, (c & 3) * C::kPages + (lane & 7));
+    const uint32_t nvalid = __popc(__ballot_sync(kFull, lane < C::kPages && mine >= 0));
+    const uint32_t bytes = nvalid * (uint32_t)L::kPage;
+    // page flags first: the arrive below releases them to the consumers
+    if (lane < C::kPages) pvalid[st * 8 + lane] = mine >= 0 ? 1 : 0;
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(bars.full(st), bytes);
+    __syncwarp();
+    // lane p issues page p's copies (one issuing thread would serialise them)
+    if (lane < C::kPages) {
+      const int id = mine;
+      if (id >= 0) {
+        const uint32_t dst = sbase + C::kRing + st * C::kStageBytes;
+        const long page = (long)id * a.Hk + kvh;
+        const uint8_t* src = a.cache + page * L::kPage;
+        if constexpr (PRESET == 0) {
+          tma_load_3d(dst + lane * C::kKeyBlock, &tmap_keys, 0, 0, (int)page, bars.full(st));
+          bulk_g2s(dst + C::kRestOff + lane * C::kRestBytes, src + C::kKeyBlock, C::kRestBytes, bars.full(st));
+        } else {
+          bulk_g2s(dst + lane * L::kPage, src, L::kPage, bars.full(st));
+        }
+      }
+    }
+    __syncwarp();
+  };
+  if (warp == 0 && nchunks > 0) fetch_ids(0);  // in flight during the set-up
+
   // ---- set-up: barriers, tensor memory
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bars.full(s), 1);
-      mbar_init(bars.empty(s), 4 * C::kW);
+      mbar_init(bars.empty(s), 4);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bars.akv(i), 4 * C::kW);
-      mbar_init(bars.qk(i), 1);
-      mbar_init(bars.sfree(i), 4 * C::kW);
-      mbar_init(bars.pfull(i), 4 * C::kW);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(bars.akv(i), 4);
       mbar_init(bars.pv(i), 1);
+      mbar_init(bars.pfull(i), 4 * C::kSW);
     }
+    for (int i = 0; i < 2; ++i) mbar_init(bars.qk(i), 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -254,112 +299,75 @@ __global__ void __launch_bounds__(Cfg<PRESET, NMMA>::kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
-  __syncthreads();  // barriers initialised
+  cta_bar();  // barriers initialised
 
-  // Producer = warp 0 (all lanes wait together; lane 0 issues the copies).
-  // Block ids are fetched 32 pages (4 chunks) at a time, one id per lane.
-  int issued = 0;
-  int ids = -1;  // this lane's block id for page 32 * (c / 4) + lane
-  auto produce = [&](int c) -> bool {
-    const int st = c % C::kStages;
-    if ((c & 3) == 0) {
-      const int lp = c * C::kPages + lane;
-      ids = -1;
-      if (lp < npages) {
-        const int id = bt[page_lo + lp];
-        ids = (id >= 0 && id < a.num_blocks) ? id : -1;
-      }
+  // the first kStages chunks need no free slot: issue them before the prologue
+  const int prefill = min(nchunks, C::kStages);
+  if (warp == 0) {
+    for (int c = 0; c < prefill; ++c) {
+      if ((c & 3) == 0 && c > 0) fetch_ids(c);
+      produce(c);
     }
-    if (c >= C::kStages && !wait_bar(bars.empty(st), ((c / C::kStages) - 1) & 1, abort_flag)) return false;
-    uint32_t bytes = 0;
-    int blk[C::kPages];
-#pragma unroll
-    for (int p = 0; p < C::kPages; ++p) {
-      blk[p] = __shfl_sync(kFull, ids, (c & 3) * C::kPages + p);
-      bytes += blk[p] >= 0 ? (uint32_t)L::kPage : 0u;
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int p = 0; p < C::kPages; ++p) pvalid[st * 8 + p] = blk[p] >= 0 ? 1 : 0;
-      mbar_arrive_expect_tx(bars.full(st), bytes);
-#pragma unroll
-      for (int p = 0; p < C::kPages; ++p) {
-        if (blk[p] >= 0) {
-          const long page = (long)blk[p] * a.Hk + kvh;
-          const uint8_t* src = a.cache + page * L::kPage;
-          const uint32_t dst = sbase + C::kRing + st * C::kStageBytes;
-          if constexpr (PRESET == 0) {
-            tma_load_3d(dst + p * C::kKeyBlock, &tmap_keys, 0, 0, (int)page, bars.full(st));
-            bulk_g2s(dst + C::kRestOff + p * C::kRestBytes, src + C::kKeyBlock, C::kRestBytes, bars.full(st));
-          } else {
-            bulk_g2s(dst + p * L::kPage, src, L::kPage, bars.full(st));
-          }
-        }
-      }
-    }
-    issued = c + 1;
-    return true;
-  };
-  if (warp == 0) {  // start streaming before the query prologue
-    for (int c = 0; c < min(nchunks, 2); ++c) produce(c);
   }
 
-  // ---- query rows (workers) and code-pair table (warps 2-3)
+  // ---- query rows (dequant + softmax warpgroups) and code-pair table (warps 2-3)
   if (tid >= 128) {
     // Q rows r = n * group + jq (zero beyond R) into the K-major, 128B-swizzled
     // B operand: row r, coordinate d at block d/64, line r, 16-byte chunk
     // ((d % 64) / 8) ^ (r % 8).  Eight threads per row, 16 coordinates each;
     // k3v4_nc rotates the rows: q_rot = H q / sqrt(128).
-    const int r = (tid - 128) >> 3, part = (tid - 128) & 7;
-    float x[16];
+    for (int item = tid - 128; item < NR * 8; item += C::kThreads - 128) {
+      const int r = item >> 3, part = item & 7;
+      float x[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) x[e] = 0.f;
-    if (r < a.R) {
-      const int n = r / a.group, jq = r % a.group;
-      const uint4* qp = reinterpret_cast<const uint4*>(
-          a.q + (((long)n * a.B + b) * a.Hq + kvh * a.group + jq) * kD + 16 * part);
+      for (int e = 0; e < 16; ++e) x[e] = 0.f;
+      if (r < a.R) {
+        const int n = r / a.group, jq = r % a.group;
+        const uint4* qp = reinterpret_cast<const uint4*>(
+            a.q + (((long)n * a.B + b) * a.Hq + kvh * a.group + jq) * kD + 16 * part);
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const uint4 v4 = qp[u];
-        const uint32_t w[4] = {v4.x, v4.y, v4.z, v4.w};
+        for (int u = 0; u < 2; ++u) {
+          const uint4 v4 = qp[u];
+          const uint32_t w[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __half2 h2 = *reinterpret_cast<const __half2*>(&w[e]);
-          x[8 * u + 2 * e] = __low2float(h2);
-          x[8 * u + 2 * e + 1] = __high2float(h2);
-        }
-      }
-    }
-    if (PRESET == 1) {
-#pragma unroll
-      for (int hs = 1; hs < 16; hs <<= 1)
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          if (!(e & hs)) {
-            const float u = x[e], v = x[e + hs];
-            x[e] = u + v;
-            x[e + hs] = u - v;
+          for (int e = 0; e < 4; ++e) {
+            const __half2 h2 = *reinterpret_cast<const __half2*>(&w[e]);
+            x[8 * u + 2 * e] = __low2float(h2);
+            x[8 * u + 2 * e + 1] = __high2float(h2);
           }
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) {  // strides 16, 32, 64: partner thread part ^ o
-        const bool upper = (part & o) != 0;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float pv = __shfl_xor_sync(kFull, x[e], o);
-          x[e] = upper ? pv - x[e] : x[e] + pv;
         }
       }
+      if (PRESET == 1) {
 #pragma unroll
-      for (int e = 0; e < 16; ++e) x[e] *= 0.08838834764831845f;
-    }
+        for (int hs = 1; hs < 16; hs <<= 1)
 #pragma unroll
-    for (int hc = 0; hc < 2; ++hc) {
-      const int d0 = 16 * part + 8 * hc;  // first coordinate of this 16-byte chunk
-      uint8_t* rowp = sm + C::kQ + (d0 >> 6) * (NMMA * 128) + (r >> 3) * 1024 + (r & 7) * 128;
-      const int chunk16 = (d0 & 63) >> 3;
-      *reinterpret_cast<uint4*>(rowp + ((chunk16 ^ (r & 7)) << 4)) =
-          make_uint4(pack_half2(x[8 * hc + 0], x[8 * hc + 1]), pack_half2(x[8 * hc + 2], x[8 * hc + 3]),
-                     pack_half2(x[8 * hc + 4], x[8 * hc + 5]), pack_half2(x[8 * hc + 6], x[8 * hc + 7]));
+          for (int e = 0; e < 16; ++e)
+            if (!(e & hs)) {
+              const float u = x[e], v = x[e + hs];
+              x[e] = u + v;
+              x[e + hs] = u - v;
+            }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {  // strides 16, 32, 64: partner thread part ^ o
+          const bool upper = (part & o) != 0;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float pv = __shfl_xor_sync(kFull, x[e], o);
+            x[e] = upper ? pv - x[e] : x[e] + pv;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] *= 0.08838834764831845f;
+      }
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        const int d0 = 16 * part + 8 * hc;  // first coordinate of this 16-byte chunk
+        uint8_t* rowp = sm + C::kQ + (d0 >> 6) * (NR * 128) + (r >> 3) * 1024 + (r & 7) * 128;
+        const int chunk16 = (d0 & 63) >> 3;
+        *reinterpret_cast<uint4*>(rowp + ((chunk16 ^ (r & 7)) << 4)) =
+            make_uint4(pack_half2(x[8 * hc + 0], x[8 * hc + 1]), pack_half2(x[8 * hc + 2], x[8 * hc + 3]),
+                       pack_half2(x[8 * hc + 4], x[8 * hc + 5]), pack_half2(x[8 * hc + 6], x[8 * hc + 7]));
+      }
     }
   } else if (PRESET == 1 && tid >= 64) {
     for (int i = tid - 64; i < 64 * 32; i += 64) {
@@ -369,7 +377,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NMMA>::kThreads, 1)
   }
   fence_async_smem();
   tc_fence_before();
-  __syncthreads();
+  cta_bar();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const float sl2 = kLog2e * 0.08838834764831845f;  // log2(e) / sqrt(128)
@@ -378,341 +386,393 @@ __global__ void __launch_bounds__(Cfg<PRESET, NMMA>::kThreads, 1)
     regs_dec<C::kRegCtl>();
     if (warp == 0) {
       // ================= producer: 8 pages per chunk into the ring
-      for (int c = issued; c < nchunks; ++c)
-        if (!produce(c)) break;
-      // drain: copies still in flight must land before the CTA can exit
-      for (int c = max(0, issued - C::kStages); c < issued; ++c)
-        wait_bar(bars.full(c % C::kStages), (c / C::kStages) & 1, abort_flag, false);
-    } else if (warp == 1 && lane == 0) {
-      // ================= MMA issuer: S^T(c) as soon as chunk c's operands are in,
-      // O^T += V^T P'^T for chunk c - 1 once its probabilities are
-      constexpr uint32_t id_qk = idesc_f16(128, NMMA, 0, 0);
-      constexpr uint32_t id_pv = idesc_f16(128, NMMA, 0, 1);
-      int last_qk = -1, last_pv = -1;
-      auto issue_pv = [&](int cc) -> bool {
-        const int bb = cc & 1;
-        if (!wait_bar(bars.pfull(bb), (cc >> 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = smem_desc(sbase + C::kP + bb * C::kPBytes + kk * 16 * C::kLine, 16, 8 * C::kLine,
-                                        C::kSwzMode);
-          mma_ts(tmem + C::kTO, tmem + C::kTAV + 64 * (cc % 3) + 8 * kk, bd, id_pv, (cc > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(bars.pv(bb));
-        last_pv = cc;
-        return true;
-      };
-      bool ok = true;
-      for (int c = 0; c < nchunks && ok; ++c) {
-        const int bb = c & 1;
-        if (!wait_bar(bars.akv(bb), (c >> 1) & 1, abort_flag)) break;
-        if (c >= 2 && !wait_bar(bars.sfree(bb), ((c - 2) >> 1) & 1, abort_flag)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = smem_desc(sbase + C::kQ + (kk >> 2) * (NMMA * 128) + (kk & 3) * 32, 16, 1024, 2);
-          mma_ts(tmem + C::kTS + NMMA * bb, tmem + C::kTAK + 64 * bb + 8 * kk, bd, id_qk, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(bars.qk(bb));
-        last_qk = c;
-        if (c >= 1) ok = issue_pv(c - 1);
+      int c = prefill;
+      for (; c < nchunks; ++c) {
+        if ((c & 3) == 0) fetch_ids(c);
+        if (!wait_bar(bars.empty(c % C::kStages), ((c / C::kStages) - 1) & 1, abort_flag)) break;
+        produce(c);
       }
-      if (ok && last_qk == nchunks - 1 && nchunks > 0) issue_pv(nchunks - 1);
-      // drain the MMAs this thread issued before tensor memory is freed
-      if (last_qk >= 0) wait_bar(bars.qk(last_qk & 1), (last_qk >> 1) & 1, abort_flag, false);
-      if (last_pv >= 0) wait_bar(bars.pv(last_pv & 1), (last_pv >> 1) & 1, abort_flag, false);
+      // drain: copies still in flight must land before the CTA can exit
+      for (int cc = max(0, c - C::kStages); cc < c; ++cc)
+        wait_bar(bars.full(cc % C::kStages), (cc / C::kStages) & 1, abort_flag, false);
+    } else if (warp == 1 || warp == 3) {
+      // ================= MMA issuers, one stream each, on two schedulers:
+      // warp 1 issues S^T(c) = K_hat Q^T, warp 3 issues O^T += V^T P'^T
+      if (lane == 0) {
+        constexpr uint32_t id_qk = idesc_f16(128, NR, 0, 0);
+        constexpr uint32_t id_pv = idesc_f16(128, NR, 0, 1);
+        constexpr uint32_t kQ1 = NR * 8;  // second 64-coordinate block of Q, in 16-byte units
+        constexpr uint32_t kL = C::kLine;  // P' line bytes: 16 lines per K-step
+        int last = -1;
+        if (warp == 1) {
+          const uint64_t q_desc = smem_desc(sbase + C::kQ, 16, 1024, 2);
+          for (int c = 0; c < nchunks; ++c) {
+            // S^T[c % 2] was read by softmax(c - 2)
+            if (c >= 2 && !wait_bar(bars.pfull((c - 2) % 3), ((c - 2) / 3) & 1, abort_flag)) break;
+            if (!wait_bar(bars.akv(c % 3), (c / 3) & 1, abort_flag)) break;
+            tc_fence_after();
+            mma_ts_x8<2, 4, 6, kQ1, kQ1 + 2, kQ1 + 4, kQ1 + 6>(tmem + C::kTS + NR * (c & 1),
+                                                               tmem + C::kTAK + 64 * (c & 1), q_desc, id_qk, 0u);
+            tc_commit(bars.qk(c & 1));
+            last = c;
+          }
+          if (last >= 0) wait_bar(bars.qk(last & 1), (last >> 1) & 1, abort_flag, false);
+        } else {
+          const uint64_t p_desc = smem_desc(sbase + C::kP, 16, 8 * C::kLine, C::kSwzMode);
+          for (int c = 0; c < nchunks; ++c) {
+            if (!wait_bar(bars.pfull(c % 3), (c / 3) & 1, abort_flag)) break;
+            tc_fence_after();
+            mma_ts_x8<kL, 2 * kL, 3 * kL, 4 * kL, 5 * kL, 6 * kL, 7 * kL>(
+                tmem + C::kTO, tmem + C::kTAV + 64 * (c % 3), p_desc + (uint64_t)(((c % 3) * C::kPBytes) >> 4), id_pv,
+                c > 0 ? 1u : 0u);
+            tc_commit(bars.pv(c % 3));
+            last = c;
+          }
+          // drain the MMAs this thread issued before tensor memory is freed
+          if (last >= 0) wait_bar(bars.pv(last % 3), (last / 3) & 1, abort_flag, false);
+        }
+      }
+      __syncwarp();
+    }
+  } else if (warp < 8) {
+    regs_dec<C::kRegDq>();
+    // ================= dequant: thread i = TMEM lane i = token i (keys,
+    // parameters) and coordinate i (values)
+    const int i = tid - 128;
+    const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
+    const int pg_i = i >> 4, off_i = i & 15;
+    for (int c = 0; c < nchunks; ++c) {
+      const int st = c % C::kStages;
+      bool ok = wait_bar(bars.full(st), (c / C::kStages) & 1, abort_flag);
+      if (ok && c >= 2) ok = wait_bar(bars.qk(c & 1), ((c - 2) >> 1) & 1, abort_flag);  // A_K[c % 2] read by S^T(c - 2)
+      // A_V[c % 3] and the parameters [c % 3] were read by P.V(c - 3) and softmax(c - 3)
+      if (ok && c >= 3) ok = wait_bar(bars.pv(c % 3), ((c - 3) / 3) & 1, abort_flag);
+      __syncwarp();
+      if (!ok) break;
+      const uint8_t* stage = sm + C::kRing + st * C::kStageBytes;
+      // page p's fields at pgf(p) + L::kVal / kScale / kZero / kNc
+      auto pgf = [&](int p) -> const uint8_t* {
+        return PRESET == 0 ? stage + C::kRestOff + p * C::kRestBytes - C::kKeyBlock : stage + p * L::kPage;
+      };
+      // keys of token i, all 128 coordinates -> A_K[c % 2]
+      const uint32_t ak = tmem + lane_q + C::kTAK + 64 * (c & 1);
+      if constexpr (PRESET == 0) {
+        // row off_i of page pg_i's key block: 16-byte chunk q sits at q ^ (off_i % 8)
+        const uint8_t* kr = stage + pg_i * C::kKeyBlock + off_i * kD;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r[32];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 w = *reinterpret_cast<const uint4*>(kr + (((4 * h + q) ^ (off_i & 7)) << 4));
+            r[8 * q + 0] = e4m3x2_to_f16x2(w.x);
+            r[8 * q + 1] = e4m3x2_to_f16x2(w.x >> 16);
+            r[8 * q + 2] = e4m3x2_to_f16x2(w.y);
+            r[8 * q + 3] = e4m3x2_to_f16x2(w.y >> 16);
+            r[8 * q + 4] = e4m3x2_to_f16x2(w.z);
+            r[8 * q + 5] = e4m3x2_to_f16x2(w.z >> 16);
+            r[8 * q + 6] = e4m3x2_to_f16x2(w.w);
+            r[8 * q + 7] = e4m3x2_to_f16x2(w.w >> 16);
+          }
+          tmem_st32(ak + 32 * h, r);
+        }
+      } else {
+        // 384 bits of 3-bit codes; pair j (coordinates 2j, 2j+1) at bits 6j .. 6j+5
+        const uint4* kw = reinterpret_cast<const uint4*>(stage + pg_i * L::kPage + L::kKey + off_i * 48);
+        uint32_t wd[13];
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+          const uint4 w = kw[u];
+          wd[4 * u + 0] = w.x;
+          wd[4 * u + 1] = w.y;
+          wd[4 * u + 2] = w.z;
+          wd[4 * u + 3] = w.w;
+        }
+        wd[12] = 0u;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r[32];
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int bit = 6 * (32 * h + jj), wi = bit >> 5, sh = bit & 31;
+            uint32_t f = wd[wi] >> sh;
+            if (sh > 26) f |= wd[wi + 1] << (32 - sh);
+            r[jj] = pairs[(f & 63u) * 32 + lane];
+          }
+          tmem_st32(ak + 32 * h, r);
+        }
+      }
+      // value codes of coordinate i, all 128 tokens -> A_V[c % 3]: word x of
+      // eight codes (token k in bits 4k .. 4k+3) gives the columns
+      // (t0, 16 t5) (16 t1, t4) (t2, 16 t7) (16 t3, t6) of its group of 8
+      const uint32_t av = tmem + lane_q + C::kTAV + 64 * (c % 3);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[32];
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+          const uint2 w = *reinterpret_cast<const uint2*>(pgf(4 * h + pp) + L::kVal + 8 * i);
+#pragma unroll
+          for (int hw = 0; hw < 2; ++hw) {
+            const uint32_t x = hw ? w.y : w.x, x8 = x >> 8;
+            r[8 * pp + 4 * hw + 0] = x & 0x00F0000Fu;
+            r[8 * pp + 4 * hw + 1] = x & 0x000F00F0u;
+            r[8 * pp + 4 * hw + 2] = x8 & 0x00F0000Fu;
+            r[8 * pp + 4 * hw + 3] = x8 & 0x000F00F0u;
+          }
+        }
+        tmem_st32(av + 32 * h, r);
+      }
+      // per-token parameters of token i
+      {
+        const int pos = (page_lo + c * C::kPages) * kBlock + i;
+        const bool valid = pvalid[st * 8 + pg_i] != 0 && pos < t_hi;
+        float cs = sl2, sv = 0.f, zv = 0.f;
+        int rmin = 1 << 20;
+        if (valid) {
+          const uint8_t* pg = pgf(pg_i);
+          if constexpr (PRESET == 1)
+            cs = __half2float(*reinterpret_cast<const __half*>(pg + L::kNc + 2 * off_i)) * sl2;
+          // odd tokens enter the value operand 16 times larger
+          sv = __half2float(*reinterpret_cast<const __half*>(pg + L::kScale + 2 * off_i)) * ((i & 1) ? 0.0625f : 1.f);
+          zv = __half2float(*reinterpret_cast<const __half*>(pg + L::kZero + 2 * off_i));
+          rmin = 0;
+          if (a.causal) {
+            const int nmin = pos - L_b + a.n_spec;  // draft n sees this token iff n >= nmin
+            rmin = nmin <= 0 ? 0 : nmin * a.group;
+          }
+        }
+        colp[(c % 3) * 128 + i] = make_float4(cs, sv, zv, __int_as_float(rmin));
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bars.akv(c % 3));
+        mbar_arrive(bars.empty(st));
+      }
     }
   } else {
-    if constexpr (C::kW > 1) regs_inc<C::kRegW>();
-    // ================= workers: thread t = TMEM lane t (token t / coordinate t)
-    const int wg = (warp - 4) >> 2;  // worker warpgroup
+    regs_inc<C::kRegSm>();
+    // ================= softmax warpgroup j: thread i = TMEM lane i = token i,
+    // query rows [row0, row0 + kRS)
+    constexpr int kH = kRS / 2;
+    const int j = (warp - 8) >> 2;
     const int sw = warp & 3;
-    const int t = sw * 32 + lane;
+    const int i = sw * 32 + lane;
     const uint32_t lane_q = (uint32_t)(sw * 32) << 16;
-    const uint32_t bar_id = 1 + wg;
-    const int pg_t = t >> 4, off_t = t & 15;  // token t of a chunk: page and row
-    // running maxima start at a finite floor: a masked score (-inf) then always
-    // gives p = 2^-inf = 0, and the first visible score forces a rescale
-    constexpr float kFloor = -1.0e30f;
-    float m[kNC], l[kNC], zs[kNC];
+    const uint32_t bar_id = 1 + j;
+    const int row0 = kRS * j;
+    float* red = reinterpret_cast<float*>(sm + C::kRed + j * C::kRedWG);  // [3][4][32], [2][32], [32]
+    // this token's line of P' (MN-major, swizzled): byte offsets of its 16-byte chunks
+    uint32_t poff[kRS / 8];
+    {
+      const int line = kappa(i);
 #pragma unroll
-    for (int r = 0; r < kNC; ++r) {
-      m[r] = kFloor;
-      l[r] = 0.f;
-      zs[r] = 0.f;
+      for (int q = 0; q < kRS / 8; ++q) {
+        const uint32_t lg = (uint32_t)((line >> 3) * (8 * C::kLine) + (line & 7) * C::kLine + row0 * 2 + 16 * q);
+        poff[q] = lg ^ (((lg >> 7) & ((1u << C::kSwzBits) - 1u)) << 4);
+      }
     }
+    // running maxima start at a finite floor: the first visible score of a row
+    // always forces the exact path
+    float2 nm[kH], l2[kH], z2[kH];  // -m, l, zero term (row pairs)
+#pragma unroll
+    for (int k = 0; k < kH; ++k) {
+      nm[k] = make_float2(1.0e30f, 1.0e30f);
+      l2[k] = make_float2(0.f, 0.f);
+      z2[k] = make_float2(0.f, 0.f);
+    }
+    const uint32_t s_base = tmem + lane_q + C::kTS + row0;
     bool aborted = false;
-    for (int it = 0; it <= nchunks; ++it) {
-      // ---------- part A: this warpgroup's share of chunk `it`'s operands
-      if (it < nchunks && !aborted) {
-        const int c = it, st = c % C::kStages, bb = c & 1;
-        bool ok = wait_bar(bars.full(st), (c / C::kStages) & 1, abort_flag);
-        if (ok && c >= 2) ok = wait_bar(bars.qk(bb), ((c - 2) >> 1) & 1, abort_flag);  // A_K[c % 2] read by S^T(c - 2)
-        // token params [c % 3] read by softmax(c - 3) before its sfree; softmax(c - 1)
-        // on the same barrier cannot finish before this warpgroup's part B of it
-        if (ok && c >= 3 && wg == 0) ok = wait_bar(bars.sfree((c - 3) & 1), ((c - 3) >> 1) & 1, abort_flag);
-        // A_V[c % 3] read by O^T(c - 3); O^T(c - 1), on the same barrier, is not
-        // issued before every worker has finished this part, so the parity is unambiguous
-        if (ok && c >= 3) ok = wait_bar(bars.pv((c - 3) & 1), ((c - 3) >> 1) & 1, abort_flag);
-        if (!ok) {
-          aborted = true;
-        } else {
-          const uint8_t* stage = sm + C::kRing + st * C::kStageBytes;
-          // page p's fields at pgf(p) + L::kVal / kScale / kZero / kNc
-          auto pgf = [&](int p) -> const uint8_t* {
-            return PRESET == 0 ? stage + C::kRestOff + p * C::kRestBytes - C::kKeyBlock : stage + p * L::kPage;
-          };
-          // keys of token t, coordinates [2 kKC wg, 2 kKC wg + 2 kKC) -> A_K[bb], lane t
-          {
-            uint32_t r[kKC];
-            if constexpr (PRESET == 0) {
-              // row off_t of page pg_t's key block: 16-byte chunk q sits at q ^ (off_t % 8)
-              const uint8_t* kr = stage + pg_t * C::kKeyBlock + off_t * kD;
+    // S^T(c) is loaded into registers one chunk ahead, while the previous
+    // chunk's P' is stored
+    // x: S^T(c) as loaded (one chunk ahead, while the previous chunk's P' is
+    // stored), then in place d = s * score_scale - m
+    uint32_t x[kRS];
+    bool pre = false;  // x already holds (or is loading) S^T(c)
+    for (int c = 0; c < nchunks; ++c) {
+      bool ok = !aborted;
+      if (!pre) {
+        ok = ok && wait_bar(bars.akv(c % 3), (c / 3) & 1, abort_flag) &&
+             wait_bar(bars.qk(c & 1), (c >> 1) & 1, abort_flag);
+        __syncwarp();
+        tc_fence_after();
+        tmem_ld<kRS>(s_base + NR * (c & 1), x);
+      }
+      tc_wait_ld();
+      const float4 cp = colp[(c % 3) * 128 + i];
+      const int rmin = __float_as_int(cp.w);
+      const bool masked = __any_sync(kFull, rmin > row0);
+      float2* d = reinterpret_cast<float2*>(x);
+      // d = s * score_scale - m, masked rows -> -inf
+      auto scores = [&]() {
+        const float2 cs2 = make_float2(cp.x, cp.x);
 #pragma unroll
-              for (int q = 0; q < kKC / 8; ++q) {
-                const int qq = (kKC / 8) * wg + q;  // logical 16-byte chunk of the row
-                const uint4 w = *reinterpret_cast<const uint4*>(kr + ((qq ^ (off_t & 7)) << 4));
-                r[8 * q + 0] = e4m3x2_to_half2(w.x);
-                r[8 * q + 1] = e4m3x2_to_half2(w.x >> 16);
-                r[8 * q + 2] = e4m3x2_to_half2(w.y);
-                r[8 * q + 3] = e4m3x2_to_half2(w.y >> 16);
-                r[8 * q + 4] = e4m3x2_to_half2(w.z);
-                r[8 * q + 5] = e4m3x2_to_half2(w.z >> 16);
-                r[8 * q + 6] = e4m3x2_to_half2(w.w);
-                r[8 * q + 7] = e4m3x2_to_half2(w.w >> 16);
-              }
-            } else {
-              // 3-bit codes of coordinates [2 kKC wg, ...) start at byte 6 kKC wg / 8
-              constexpr int kWords = 6 * kKC / 32;
-              const uint32_t* kw = reinterpret_cast<const uint32_t*>(stage + pg_t * L::kPage + L::kKey + off_t * 48 +
-                                                                     (6 * kKC / 8) * wg);
-              uint32_t wd[kWords + 1];
+        for (int k = 0; k < kH; ++k)
+          d[k] = __ffma2_rn(make_float2(__uint_as_float(x[2 * k]), __uint_as_float(x[2 * k + 1])), cs2, nm[k]);
+        if (masked) {
 #pragma unroll
-              for (int u = 0; u < kWords; ++u) wd[u] = kw[u];
-              wd[kWords] = 0u;
-#pragma unroll
-              for (int jj = 0; jj < kKC; ++jj) {  // pair jj: codes of 2jj, 2jj+1 at bits 6jj .. 6jj+5
-                const int bit = 6 * jj, wi = bit >> 5, sh = bit & 31;
-                uint32_t f = wd[wi] >> sh;
-                if (sh > 26) f |= wd[wi + 1] << (32 - sh);
-                r[jj] = pairs[(f & 63u) * 32 + lane];
-              }
-            }
-            tmem_st_cols<kKC>(tmem + lane_q + C::kTAK + 64 * bb + kKC * wg, r);
-          }
-          // value codes of coordinate t, tokens [2 kKC wg, ...) = pages [kKC wg / 8, ...) -> A_V[bb]
-          {
-            uint32_t r[kKC];
-#pragma unroll
-            for (int pp = 0; pp < kKC / 8; ++pp) {
-              const int p = (kKC / 8) * wg + pp;
-              const uint2 w = *reinterpret_cast<const uint2*>(pgf(p) + L::kVal + 8 * t);
-#pragma unroll
-              for (int half = 0; half < 2; ++half) {
-                const uint32_t x = half ? w.y : w.x;  // 4 bytes: token pairs of this coordinate
-                const uint32_t lo = x & 0x0F0F0F0Fu, hi = (x >> 4) & 0x0F0F0F0Fu;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const uint32_t y = __byte_perm(lo, hi, (uint32_t)k | ((uint32_t)(4 + k) << 8));
-                  r[8 * pp + 4 * half + k] = y & 0x000F000Fu;  // fp16 bits = code: code * 2^-24
-                }
-              }
-            }
-            tmem_st_cols<kKC>(tmem + lane_q + C::kTAV + 64 * (c % 3) + kKC * wg, r);
-          }
-          // per-token parameters of token t (warpgroup 0)
-          if (wg == 0) {
-            const int pos = (page_lo + c * C::kPages) * kBlock + t;
-            const bool valid = pvalid[st * 8 + pg_t] != 0 && pos < t_hi;
-            float cs = sl2, sv = 0.f, zv = 0.f;
-            int rmin = 1 << 20;
-            if (valid) {
-              const uint8_t* pg = pgf(pg_t);
-              if constexpr (PRESET == 1)
-                cs = __half2float(*reinterpret_cast<const __half*>(pg + L::kNc + 2 * off_t)) * sl2;
-              sv = __half2float(*reinterpret_cast<const __half*>(pg + L::kScale + 2 * off_t));
-              zv = __half2float(*reinterpret_cast<const __half*>(pg + L::kZero + 2 * off_t));
-              rmin = 0;
-              if (a.causal) {
-                const int nmin = pos - L_b + a.n_spec;  // draft n sees this token iff n >= nmin
-                rmin = nmin <= 0 ? 0 : nmin * a.group;
-              }
-            }
-            colp[(c % 3) * 128 + t] = make_float4(cs, sv, zv, __int_as_float(rmin));
-          }
-          tc_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(bars.akv(bb));
-            mbar_arrive(bars.empty(st));
+          for (int k = 0; k < kH; ++k) {
+            if (row0 + 2 * k < rmin) d[k].x = -CUDART_INF_F;
+            if (row0 + 2 * k + 1 < rmin) d[k].y = -CUDART_INF_F;
           }
         }
+      };
+      scores();
+      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+      for (int k = 0; k < kH; k += 2) {
+        mx0 = fmax3(mx0, d[k].x, d[k].y);
+        if (k + 1 < kH) mx1 = fmax3(mx1, d[k + 1].x, d[k + 1].y);
       }
-      // ---------- part B: softmax of chunk it - 1 for rows [16 wg, 16 wg + 16)
-      if (it >= 1) {
-        const int c = it - 1, bb = c & 1;
-        const bool ok = !aborted && wait_bar(bars.qk(bb), (c >> 1) & 1, abort_flag) &&
-                        wait_bar(bars.akv(bb), (c >> 1) & 1, abort_flag);
-        // leave the loop together: the named barriers below need all four warps
-        if (bar_red_or(bar_id, 128, !ok || aborted)) {
+      // leave the loop together: the named barriers need all four warps
+      if (bar_red_or(bar_id, 128, fmaxf(mx0, mx1) > kRescaleThreshold || !ok)) {
+        if (bar_red_or(bar_id, 128, !ok)) {
           aborted = true;
           break;
         }
-        tc_fence_after();
-        const float4 cp = colp[(c % 3) * 128 + t];
-        const int rmin = __float_as_int(cp.w);
-        const uint32_t s_addr = tmem + lane_q + C::kTS + NMMA * bb + kNC * wg;
-        float y[kNC];
-        auto load_scores = [&]() {
-          uint32_t r[kNC];
-          tmem_ld<kNC>(s_addr, r);
+        // exact maximum of this chunk for each row over the 128 tokens
+        // the raw scores again (S^T(c) stays valid until this chunk's pfull)
+        tmem_ld<kRS>(s_base + NR * (c & 1), x);
+        tc_wait_ld();
+        float v[kRS];
+#pragma unroll
+        for (int k = 0; k < kRS; ++k) v[k] = (masked && row0 + k < rmin) ? -CUDART_INF_F : __uint_as_float(x[k]) * cp.x;
+        warp_transpose_reduce<kRS, true>(v, lane);
+        float* rmax = red;  // [4][32]
+        if (lane < kRS) rmax[sw * 32 + lane] = v[0];
+        named_bar(bar_id, 128);
+        float* ral = red + 3 * 4 * 32 + 2 * 32;  // [32] rescale factors of this chunk
+        bool change = false;
+#pragma unroll
+        for (int k = 0; k < kH; ++k) {
+          const float cm0 = fmaxf(fmaxf(rmax[2 * k], rmax[32 + 2 * k]), fmaxf(rmax[64 + 2 * k], rmax[96 + 2 * k]));
+          const float cm1 =
+              fmaxf(fmaxf(rmax[2 * k + 1], rmax[33 + 2 * k]), fmaxf(rmax[65 + 2 * k], rmax[97 + 2 * k]));
+          const float mo0 = -nm[k].x, mo1 = -nm[k].y;
+          const float mn0 = fmaxf(mo0, cm0), mn1 = fmaxf(mo1, cm1);
+          const float2 a2 = make_float2(ex2(mo0 - mn0), ex2(mo1 - mn1));
+          change |= (mn0 > mo0) || (mn1 > mo1);
+          nm[k] = make_float2(-mn0, -mn1);
+          l2[k] = __fmul2_rn(l2[k], a2);
+          z2[k] = __fmul2_rn(z2[k], a2);
+          if (i == 2 * k) ral[2 * k] = a2.x;
+          if (i == 2 * k + 1) ral[2 * k + 1] = a2.y;
+        }
+        named_bar(bar_id, 128);  // ral is complete; rmax may be reused
+        if (change && c > 0) {  // uniform across the warpgroup
+          // O^T holds chunks < c: rescale it after P.V(c - 1) has landed and
+          // before P.V(c) is issued (which needs this warpgroup's pfull)
+          if (!wait_bar(bars.pv((c - 1) % 3), ((c - 1) / 3) & 1, abort_flag)) aborted = true;
+          __syncwarp();
+          tc_fence_after();
+          const uint32_t o_addr = tmem + lane_q + C::kTO + row0;
+          uint32_t o[kRS];
+          tmem_ld<kRS>(o_addr, o);
           tc_wait_ld();
-          if (__all_sync(kFull, rmin <= kNC * wg)) {  // every row of this warpgroup sees these tokens
 #pragma unroll
-            for (int k = 0; k < kNC; ++k) y[k] = __uint_as_float(r[k]) * cp.x;
-          } else {
-#pragma unroll
-            for (int k = 0; k < kNC; ++k)
-              y[k] = (kNC * wg + k < rmin) ? -CUDART_INF_F : __uint_as_float(r[k]) * cp.x;
-          }
-        };
-        load_scores();
-        bool need = false;
-#pragma unroll
-        for (int k = 0; k < kNC; ++k) need |= y[k] > m[k] + kRescaleThreshold;
-        need = bar_red_or(bar_id, 128, need);
-        if (need) {
-          // exact maximum of this chunk for each row over the 128 tokens
-          // (reduces y in place; the scores are reloaded from tensor memory)
-          warp_transpose_reduce<kNC, true>(y, lane);
-          float* rmax = red + (wg * 3 + 0) * 4 * kNC;
-          if (lane < kNC) rmax[sw * kNC + lane] = y[0];
-          named_bar(bar_id, 128);
-#pragma unroll
-          for (int k = 0; k < kNC; ++k)
-            y[k] = fmaxf(fmaxf(rmax[k], rmax[kNC + k]), fmaxf(rmax[2 * kNC + k], rmax[3 * kNC + k]));
-          bool change = false;
-#pragma unroll
-          for (int k = 0; k < kNC; ++k) change |= y[k] > m[k];
-          const bool rescale_o = change && c > 0;  // uniform across the warpgroup
-          if (rescale_o) {
-            // O^T holds chunks < c: rescale it after the previous P.V has landed
-            // and before this chunk's is issued
-            if (!wait_bar(bars.pv((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag)) aborted = true;
-            tc_fence_after();
-          }
-          uint32_t r[kNC];
-          const uint32_t o_addr = tmem + lane_q + C::kTO + kNC * wg;
-          if (rescale_o) {
-            tmem_ld<kNC>(o_addr, r);
-            tc_wait_ld();
-          }
-#pragma unroll
-          for (int k = 0; k < kNC; ++k) {
-            const float mn = fmaxf(m[k], y[k]);
-            const float al = ex2(m[k] - mn);
-            m[k] = mn;
-            l[k] *= al;
-            zs[k] *= al;
-            r[k] = __float_as_uint(__uint_as_float(r[k]) * al);
-          }
-          if (rescale_o) {
-            tmem_st<kNC>(o_addr, r);
-            tc_wait_st();
-          }
-          load_scores();
+          for (int k = 0; k < kRS; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * ral[k]);
+          tmem_st<kRS>(o_addr, o);
+          tc_wait_st();
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.sfree(bb));
-        if (c >= 2 && !wait_bar(bars.pv(bb), ((c - 2) >> 1) & 1, abort_flag)) aborted = true;
-        // probabilities, row sums, zero term; P' = p * scale into the MN-major B tile
-        uint8_t* pbuf = sm + C::kP + bb * C::kPBytes;
-#pragma unroll
-        for (int q = 0; q < kNC / 8; ++q) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int k = 8 * q + 2 * e;
-            const float p0 = ex2(y[k] - m[k]);
-            const float p1 = ex2(y[k + 1] - m[k + 1]);
-            l[k] += p0;
-            l[k + 1] += p1;
-            zs[k] = fmaf(p0, cp.z, zs[k]);
-            zs[k + 1] = fmaf(p1, cp.z, zs[k + 1]);
-            pk[e] = pack_half2(p0 * cp.y, p1 * cp.y);
-          }
-          const uint32_t lg = (uint32_t)((t >> 3) * (8 * C::kLine) + (t & 7) * C::kLine + wg * kNC * 2 + 16 * q);
-          const uint32_t ph = lg ^ (((lg >> 7) & ((1u << C::kSwzBits) - 1u)) << 4);
-          *reinterpret_cast<uint4*>(pbuf + ph) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.pfull(bb));
+        scores();
       }
+      // probabilities, row sums, zero term; P' = p * scale into the MN-major B tile
+      uint32_t pk[kH];
+      const float2 sv2 = make_float2(cp.y, cp.y), zv2 = make_float2(cp.z, cp.z);
+#pragma unroll
+      for (int k = 0; k < kH; ++k) {
+        const float2 p = make_float2(ex2(d[k].x), ex2(d[k].y));
+        l2[k] = __fadd2_rn(l2[k], p);
+        z2[k] = __ffma2_rn(p, zv2, z2[k]);
+        const float2 ps = __fmul2_rn(p, sv2);
+        pk[k] = pack_half2(ps.x, ps.y);
+      }
+      // start loading S^T(c + 1) if it is already there (never wait for it here:
+      // this chunk's pfull would then depend on S^T(c + 1))
+      pre = false;
+      if (c + 1 < nchunks) {
+        const int cn = c + 1;
+        const bool rdy = mbar_test_wait(bars.akv(cn % 3), (cn / 3) & 1) && mbar_test_wait(bars.qk(cn & 1), (cn >> 1) & 1);
+        if (__all_sync(kFull, rdy)) {
+          tc_fence_after();
+          tmem_ld<kRS>(s_base + NR * (cn & 1), x);
+          pre = true;
+        }
+      }
+      // P'[c % 3] was read by P.V(c - 3)
+      if (c >= 3 && !wait_bar(bars.pv(c % 3), ((c - 3) / 3) & 1, abort_flag)) aborted = true;
+      uint8_t* pbuf = sm + C::kP + (c % 3) * C::kPBytes;
+#pragma unroll
+      for (int q = 0; q < kRS / 8; ++q)
+        *reinterpret_cast<uint4*>(pbuf + poff[q]) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.pfull(c % 3));
     }
     // ---- epilogue: l and zero term over all 128 tokens, then O^T / l
     {
-      float v[kNC];
+      float v[kRS];
 #pragma unroll
-      for (int k = 0; k < kNC; ++k) v[k] = l[k];
-      warp_transpose_reduce<kNC, false>(v, lane);
-      float* rl = red + (wg * 3 + 1) * 4 * kNC;
-      if (lane < kNC) rl[sw * kNC + lane] = v[0];
+      for (int k = 0; k < kH; ++k) {
+        v[2 * k] = l2[k].x;
+        v[2 * k + 1] = l2[k].y;
+      }
+      warp_transpose_reduce<kRS, false>(v, lane);
+      if (lane < kRS) red[(4 + sw) * 32 + lane] = v[0];
 #pragma unroll
-      for (int k = 0; k < kNC; ++k) v[k] = zs[k];
-      warp_transpose_reduce<kNC, false>(v, lane);
-      float* rz = red + (wg * 3 + 2) * 4 * kNC;
-      if (lane < kNC) rz[sw * kNC + lane] = v[0];
+      for (int k = 0; k < kH; ++k) {
+        v[2 * k] = z2[k].x;
+        v[2 * k + 1] = z2[k].y;
+      }
+      warp_transpose_reduce<kRS, false>(v, lane);
+      if (lane < kRS) red[(8 + sw) * 32 + lane] = v[0];
     }
     named_bar(bar_id, 128);
-    uint32_t o[kNC];
+    uint32_t o[kRS];
 #pragma unroll
-    for (int k = 0; k < kNC; ++k) o[k] = 0u;
-    if (nchunks > 0 && !aborted) {
+    for (int k = 0; k < kRS; ++k) o[k] = 0u;
+    if (nchunks > 0) {
       const int lc = nchunks - 1;
-      if (wait_bar(bars.pv(lc & 1), (lc >> 1) & 1, abort_flag)) {
-        tc_fence_after();
-        tmem_ld<kNC>(tmem + lane_q + C::kTO + kNC * wg, o);
-        tc_wait_ld();
-      } else {
-        aborted = true;
-      }
+      if (!aborted && !wait_bar(bars.pv(lc % 3), (lc / 3) & 1, abort_flag)) aborted = true;
+      __syncwarp();
+      tc_fence_after();
+      tmem_ld<kRS>(tmem + lane_q + C::kTO + row0, o);  // read even after an abort: warp-collective
+      tc_wait_ld();
     }
     aborted = aborted || (*abort_flag != 0u);
-    // per-row constants (threads 0..15): 1 / l, zero term / l, log-sum-exp
-    float* rowc = red + C::kW * 3 * 4 * kNC + wg * 2 * kNC;
-    if (t < kNC) {
-      const float* rl = red + (wg * 3 + 1) * 4 * kNC;
-      const float* rz = red + (wg * 3 + 2) * 4 * kNC;
-      const float lt = (rl[t] + rl[kNC + t]) + (rl[2 * kNC + t] + rl[3 * kNC + t]);
-      const float zt = (rz[t] + rz[kNC + t]) + (rz[2 * kNC + t] + rz[3 * kNC + t]);
-      float mt = m[0];
+    // per-row constants (threads 0 .. kRS-1): 1 / l, zero term / l, log-sum-exp
+    float* rowc = red + 3 * 4 * 32;
+    if (i < kRS) {
+      const float* rl = red + 4 * 32;
+      const float* rz = red + 8 * 32;
+      const float lt = (rl[i] + rl[32 + i]) + (rl[64 + i] + rl[96 + i]);
+      const float zt = (rz[i] + rz[32 + i]) + (rz[64 + i] + rz[96 + i]);
+      float mt = -nm[0].x;
 #pragma unroll
-      for (int k = 1; k < kNC; ++k) mt = (t == k) ? m[k] : mt;
+      for (int k = 1; k < kRS; ++k) mt = (i == k) ? -((k & 1) ? nm[k >> 1].y : nm[k >> 1].x) : mt;
       const float inv = lt > 0.f ? 1.0f / lt : 0.f;
-      rowc[t] = inv * 16777216.0f;  // O^T holds the value codes as fp16 subnormals (code * 2^-24)
-      rowc[kNC + t] = zt * inv;
-      const int row = kNC * wg + t;
+      rowc[i] = inv * 16777216.0f;  // O^T holds the value codes as fp16 subnormals (code * 2^-24)
+      rowc[32 + i] = zt * inv;
+      const int row = row0 + i;
       if (row < a.R) {
         const long orow = (((long)(row / a.group) * a.B + b) * a.Hq + kvh * a.group + row % a.group) * a.S + split;
         a.part_lse[orow] = aborted ? CUDART_NAN_F : (lt > 0.f ? (mt + log2f(lt)) * kLn2 : -CUDART_INF_F);
       }
     }
     named_bar(bar_id, 128);
-    // rows 16 wg + k = n * group + j, walked incrementally
-    int jj = (kNC * wg) % a.group;
-    float* po = a.part_o + ((((long)((kNC * wg) / a.group) * a.B + b) * a.Hq + kvh * a.group + jj) * a.S + split) * kD + t;
+    // rows row0 + k = n * group + jq, walked incrementally; thread i writes coordinate i
+    int jq = row0 % a.group;
+    float* po = a.part_o + ((((long)(row0 / a.group) * a.B + b) * a.Hq + kvh * a.group + jq) * a.S + split) * kD + i;
     const long step_j = (long)a.S * kD, step_n = ((long)a.B * a.Hq - a.group) * a.S * kD;
 #pragma unroll
-    for (int k = 0; k < kNC; ++k) {
-      if (kNC * wg + k < a.R) *po = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rowc[k], rowc[kNC + k]);
+    for (int k = 0; k < kRS; ++k) {
+      if (row0 + k < a.R) *po = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rowc[k], rowc[32 + k]);
       po += step_j;
-      if (++jj == a.group) {
-        jj = 0;
+      if (++jq == a.group) {
+        jq = 0;
         po += step_n;
       }
     }
@@ -720,7 +780,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NMMA>::kThreads, 1)
 
   // ---- teardown: every role has drained its asynchronous work
   tc_fence_before();
-  __syncthreads();
+  cta_bar();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
@@ -755,10 +815,10 @@ cudaError_t make_key_map(const VerifyArgs& a, CUtensorMap* m) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int PRESET, int NMMA>
+template <int PRESET, int NR>
 cudaError_t launch_tc(const VerifyArgs& a, cudaStream_t st) {
-  using C = Cfg<PRESET, NMMA>;
-  auto kern = verify_stage1_tc_kernel<PRESET, NMMA>;
+  using C = Cfg<PRESET, NR>;
+  auto kern = verify_stage1_tc_kernel<PRESET, NR>;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
