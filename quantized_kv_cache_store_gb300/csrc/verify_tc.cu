@@ -103,9 +103,13 @@ struct Cfg {
   static constexpr int kP = kQ + align_up(kQBytes, 1024);
   static constexpr int kPBytes = kTok * kLine;  // one buffer
   static constexpr int kCol = kP + 3 * kPBytes;  // float4 [3][128]: score scale, P' scale, v zero, first row
-  static constexpr int kRed = kCol + 3 * kTok * 16;  // per softmax warpgroup: float [3][4][32] + [2][32] + [32]
-  static constexpr int kRedWG = (3 * 4 * 32 + 2 * 32 + 32) * 4;
-  static constexpr int kPair = kRed + kSW * kRedWG;  // u32 [64][32] (k3v4_nc)
+  // per softmax warpgroup: -m [32], rescale factors [32], row constants [32][2]
+  static constexpr int kRed = kCol + 3 * kTok * 16;
+  static constexpr int kRedWG = 128 * 4;
+  // per softmax warpgroup: float [32 rows][128 tokens or coordinates] for transposes
+  static constexpr int kScr = kRed + kSW * kRedWG;
+  static constexpr int kScrWG = 32 * 128 * 4;
+  static constexpr int kPair = kScr + kSW * kScrWG;  // u32 [64][32] (k3v4_nc)
   static constexpr int kPValid = kPair + (PRESET == 1 ? 64 * 32 * 4 : 0);  // u8 [kStages][8]
   static constexpr int kBar = align_up(kPValid + kStages * 8, 8);
   // full[kStages] empty[kStages] akv[3] qk[2] pfull[3] pv[3]
@@ -198,6 +202,19 @@ __device__ __forceinline__ void warp_transpose_reduce(float (&v)[NC], int lane) 
       v[0] = MAX ? fmaxf(v[0], recv) : v[0] + recv;
     }
   }
+}
+
+// Transposes through shared memory ([32 rows][128 tokens] of floats): token t
+// of row k sits in 16-byte slot ((t / 4) % 8) ^ (4 (k % 2) + t / 32) of the
+// row's quarter t / 32, so that writes of one row by 32 consecutive tokens and
+// reads of row segments (thread -> row i / 4, quarter i % 4) are both free of
+// bank conflicts.
+__device__ __forceinline__ int tr_index(int k, int t) {
+  const int qt = t >> 5;
+  return k * 128 + 32 * qt + 4 * (((t >> 2) & 7) ^ (4 * (k & 1) + qt)) + (t & 3);
+}
+__device__ __forceinline__ const float4* tr_seg(const float* base, int k, int qt, int u) {
+  return reinterpret_cast<const float4*>(base + k * 128 + 32 * qt + 4 * (u ^ (4 * (k & 1) + qt)));
 }
 
 // Position of chunk token t on the K axis of the P.V contraction.  Within
@@ -563,7 +580,12 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     const uint32_t lane_q = (uint32_t)(sw * 32) << 16;
     const uint32_t bar_id = 1 + j;
     const int row0 = kRS * j;
-    float* red = reinterpret_cast<float*>(sm + C::kRed + j * C::kRedWG);  // [3][4][32], [2][32], [32]
+    float* nms = reinterpret_cast<float*>(sm + C::kRed + j * C::kRedWG);  // -m per row
+    float* als = nms + 32;                                                 // rescale factor per row
+    float2* rcs = reinterpret_cast<float2*>(nms + 64);                     // (1/l * 2^24, zero term / l)
+    float* scr = reinterpret_cast<float*>(sm + C::kScr + j * C::kScrWG);  // [32][128]
+    // row reductions through scr: thread i sums row rr over tokens [32 qt, 32 qt + 32)
+    const int rr = i >> 2, qt = i & 3;
     // this token's line of P' (MN-major, swizzled): byte offsets of its 16-byte chunks
     uint32_t poff[kRS / 8];
     {
@@ -574,19 +596,18 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         poff[q] = lg ^ (((lg >> 7) & ((1u << C::kSwzBits) - 1u)) << 4);
       }
     }
-    // running maxima start at a finite floor: the first visible score of a row
-    // always forces the exact path
-    float2 nm[kH], l2[kH], z2[kH];  // -m, l, zero term (row pairs)
+    // running maxima (shared by the warpgroup) start at a finite floor: the
+    // first visible score of a row always forces the exact path
+    if (i < kRS) nms[i] = 1.0e30f;
+    float2 l2[kH], z2[kH];  // l and the zero term of this token's rows (row pairs)
 #pragma unroll
     for (int k = 0; k < kH; ++k) {
-      nm[k] = make_float2(1.0e30f, 1.0e30f);
       l2[k] = make_float2(0.f, 0.f);
       z2[k] = make_float2(0.f, 0.f);
     }
+    named_bar(bar_id, 128);
     const uint32_t s_base = tmem + lane_q + C::kTS + row0;
     bool aborted = false;
-    // S^T(c) is loaded into registers one chunk ahead, while the previous
-    // chunk's P' is stored
     // x: S^T(c) as loaded (one chunk ahead, while the previous chunk's P' is
     // stored), then in place d = s * score_scale - m
     uint32_t x[kRS];
@@ -608,9 +629,15 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       // d = s * score_scale - m, masked rows -> -inf
       auto scores = [&]() {
         const float2 cs2 = make_float2(cp.x, cp.x);
+        const float4* n4 = reinterpret_cast<const float4*>(nms);
 #pragma unroll
-        for (int k = 0; k < kH; ++k)
-          d[k] = __ffma2_rn(make_float2(__uint_as_float(x[2 * k]), __uint_as_float(x[2 * k + 1])), cs2, nm[k]);
+        for (int q = 0; q < kRS / 4; ++q) {
+          const float4 nv = n4[q];
+          d[2 * q] = __ffma2_rn(make_float2(__uint_as_float(x[4 * q]), __uint_as_float(x[4 * q + 1])), cs2,
+                                make_float2(nv.x, nv.y));
+          d[2 * q + 1] = __ffma2_rn(make_float2(__uint_as_float(x[4 * q + 2]), __uint_as_float(x[4 * q + 3])), cs2,
+                                    make_float2(nv.z, nv.w));
+        }
         if (masked) {
 #pragma unroll
           for (int k = 0; k < kH; ++k) {
@@ -632,48 +659,62 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
           aborted = true;
           break;
         }
-        // exact maximum of this chunk for each row over the 128 tokens
-        // the raw scores again (S^T(c) stays valid until this chunk's pfull)
+        // exact maximum of this chunk for each row over the 128 tokens: the
+        // raw scaled scores (S^T(c) stays valid until this chunk's pfull) are
+        // transposed through scr and reduced per row
         tmem_ld<kRS>(s_base + NR * (c & 1), x);
         tc_wait_ld();
-        float v[kRS];
 #pragma unroll
-        for (int k = 0; k < kRS; ++k) v[k] = (masked && row0 + k < rmin) ? -CUDART_INF_F : __uint_as_float(x[k]) * cp.x;
-        warp_transpose_reduce<kRS, true>(v, lane);
-        float* rmax = red;  // [4][32]
-        if (lane < kRS) rmax[sw * 32 + lane] = v[0];
+        for (int k = 0; k < kRS; ++k)
+          scr[tr_index(k, i)] = (masked && row0 + k < rmin) ? -CUDART_INF_F : __uint_as_float(x[k]) * cp.x;
         named_bar(bar_id, 128);
-        float* ral = red + 3 * 4 * 32 + 2 * 32;  // [32] rescale factors of this chunk
-        bool change = false;
-#pragma unroll
-        for (int k = 0; k < kH; ++k) {
-          const float cm0 = fmaxf(fmaxf(rmax[2 * k], rmax[32 + 2 * k]), fmaxf(rmax[64 + 2 * k], rmax[96 + 2 * k]));
-          const float cm1 =
-              fmaxf(fmaxf(rmax[2 * k + 1], rmax[33 + 2 * k]), fmaxf(rmax[65 + 2 * k], rmax[97 + 2 * k]));
-          const float mo0 = -nm[k].x, mo1 = -nm[k].y;
-          const float mn0 = fmaxf(mo0, cm0), mn1 = fmaxf(mo1, cm1);
-          const float2 a2 = make_float2(ex2(mo0 - mn0), ex2(mo1 - mn1));
-          change |= (mn0 > mo0) || (mn1 > mo1);
-          nm[k] = make_float2(-mn0, -mn1);
-          l2[k] = __fmul2_rn(l2[k], a2);
-          z2[k] = __fmul2_rn(z2[k], a2);
-          if (i == 2 * k) ral[2 * k] = a2.x;
-          if (i == 2 * k + 1) ral[2 * k + 1] = a2.y;
+        if (rr < kRS) {
+          float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;
+#pragma unroll 1
+          for (int u = 0; u < 8; u += 2) {
+            const float4 a0 = *tr_seg(scr, rr, qt, u), a1 = *tr_seg(scr, rr, qt, u + 1);
+            m0 = fmax3(m0, fmaxf(a0.x, a0.y), fmaxf(a0.z, a0.w));
+            m1 = fmax3(m1, fmaxf(a1.x, a1.y), fmaxf(a1.z, a1.w));
+          }
+          float cm = fmaxf(m0, m1);
+          cm = fmaxf(cm, __shfl_xor_sync(kFull, cm, 1));
+          cm = fmaxf(cm, __shfl_xor_sync(kFull, cm, 2));
+          if (qt == 0) {
+            const float mo = -nms[rr], mn = fmaxf(mo, cm);
+            als[rr] = ex2(mo - mn);
+            nms[rr] = -mn;
+          }
         }
-        named_bar(bar_id, 128);  // ral is complete; rmax may be reused
+        named_bar(bar_id, 128);  // -m and the factors are complete
+        bool change = false;
+        {
+          const float4* a4 = reinterpret_cast<const float4*>(als);
+#pragma unroll
+          for (int q = 0; q < kRS / 4; ++q) {
+            const float4 a = a4[q];
+            l2[2 * q] = __fmul2_rn(l2[2 * q], make_float2(a.x, a.y));
+            z2[2 * q] = __fmul2_rn(z2[2 * q], make_float2(a.x, a.y));
+            l2[2 * q + 1] = __fmul2_rn(l2[2 * q + 1], make_float2(a.z, a.w));
+            z2[2 * q + 1] = __fmul2_rn(z2[2 * q + 1], make_float2(a.z, a.w));
+            change |= fminf(fminf(a.x, a.y), fminf(a.z, a.w)) < 1.0f;
+          }
+        }
         if (change && c > 0) {  // uniform across the warpgroup
           // O^T holds chunks < c: rescale it after P.V(c - 1) has landed and
           // before P.V(c) is issued (which needs this warpgroup's pfull)
           if (!wait_bar(bars.pv((c - 1) % 3), ((c - 1) / 3) & 1, abort_flag)) aborted = true;
           __syncwarp();
           tc_fence_after();
-          const uint32_t o_addr = tmem + lane_q + C::kTO + row0;
-          uint32_t o[kRS];
-          tmem_ld<kRS>(o_addr, o);
-          tc_wait_ld();
+#pragma unroll 1
+          for (int g = 0; g < kRS / 8; ++g) {
+            const uint32_t o_addr = tmem + lane_q + C::kTO + row0 + 8 * g;
+            uint32_t o[8];
+            tmem_ld8(o_addr, o);
+            tc_wait_ld();
 #pragma unroll
-          for (int k = 0; k < kRS; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * ral[k]);
-          tmem_st<kRS>(o_addr, o);
+            for (int e = 0; e < 8; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * als[8 * g + e]);
+            tmem_st8(o_addr, o);
+          }
           tc_wait_st();
         }
         scores();
@@ -712,69 +753,88 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.pfull(c % 3));
     }
-    // ---- epilogue: l and zero term over all 128 tokens, then O^T / l
-    {
-      float v[kRS];
+    if (pre) tc_wait_ld();
+    // ---- epilogue: l and the zero term over all 128 tokens (transposed through
+    // scr), then the output rows O^T / l staged in scr and stored in bulk
+    float lrow = 0.f, zrow = 0.f;  // row rr, in threads with qt == 0
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+      named_bar(bar_id, 128);  // scr is free
 #pragma unroll
       for (int k = 0; k < kH; ++k) {
-        v[2 * k] = l2[k].x;
-        v[2 * k + 1] = l2[k].y;
+        const float2 v = pass ? z2[k] : l2[k];
+        scr[tr_index(2 * k, i)] = v.x;
+        scr[tr_index(2 * k + 1, i)] = v.y;
       }
-      warp_transpose_reduce<kRS, false>(v, lane);
-      if (lane < kRS) red[(4 + sw) * 32 + lane] = v[0];
-#pragma unroll
-      for (int k = 0; k < kH; ++k) {
-        v[2 * k] = z2[k].x;
-        v[2 * k + 1] = z2[k].y;
+      named_bar(bar_id, 128);
+      if (rr < kRS) {
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll 1
+        for (int u = 0; u < 8; u += 2) {
+          const float4 a0 = *tr_seg(scr, rr, qt, u), a1 = *tr_seg(scr, rr, qt, u + 1);
+          s0 += (a0.x + a0.y) + (a0.z + a0.w);
+          s1 += (a1.x + a1.y) + (a1.z + a1.w);
+        }
+        float sum = s0 + s1;
+        sum += __shfl_xor_sync(kFull, sum, 1);
+        sum += __shfl_xor_sync(kFull, sum, 2);
+        if (pass) zrow = sum;
+        else lrow = sum;
       }
-      warp_transpose_reduce<kRS, false>(v, lane);
-      if (lane < kRS) red[(8 + sw) * 32 + lane] = v[0];
     }
-    named_bar(bar_id, 128);
-    uint32_t o[kRS];
-#pragma unroll
-    for (int k = 0; k < kRS; ++k) o[k] = 0u;
     if (nchunks > 0) {
       const int lc = nchunks - 1;
       if (!aborted && !wait_bar(bars.pv(lc % 3), (lc / 3) & 1, abort_flag)) aborted = true;
       __syncwarp();
       tc_fence_after();
-      tmem_ld<kRS>(tmem + lane_q + C::kTO + row0, o);  // read even after an abort: warp-collective
-      tc_wait_ld();
     }
     aborted = aborted || (*abort_flag != 0u);
-    // per-row constants (threads 0 .. kRS-1): 1 / l, zero term / l, log-sum-exp
-    float* rowc = red + 3 * 4 * 32;
-    if (i < kRS) {
-      const float* rl = red + 4 * 32;
-      const float* rz = red + 8 * 32;
-      const float lt = (rl[i] + rl[32 + i]) + (rl[64 + i] + rl[96 + i]);
-      const float zt = (rz[i] + rz[32 + i]) + (rz[64 + i] + rz[96 + i]);
-      float mt = -nm[0].x;
-#pragma unroll
-      for (int k = 1; k < kRS; ++k) mt = (i == k) ? -((k & 1) ? nm[k >> 1].y : nm[k >> 1].x) : mt;
-      const float inv = lt > 0.f ? 1.0f / lt : 0.f;
-      rowc[i] = inv * 16777216.0f;  // O^T holds the value codes as fp16 subnormals (code * 2^-24)
-      rowc[32 + i] = zt * inv;
-      const int row = row0 + i;
+    if (rr < kRS && qt == 0) {
+      const float inv = lrow > 0.f ? 1.0f / lrow : 0.f;
+      rcs[rr] = make_float2(inv * 16777216.0f, zrow * inv);  // O^T holds codes as fp16 subnormals (code * 2^-24)
+      const int row = row0 + rr;
       if (row < a.R) {
         const long orow = (((long)(row / a.group) * a.B + b) * a.Hq + kvh * a.group + row % a.group) * a.S + split;
-        a.part_lse[orow] = aborted ? CUDART_NAN_F : (lt > 0.f ? (mt + log2f(lt)) * kLn2 : -CUDART_INF_F);
+        a.part_lse[orow] = aborted ? CUDART_NAN_F : (lrow > 0.f ? (-nms[rr] + log2f(lrow)) * kLn2 : -CUDART_INF_F);
+      }
+    }
+    named_bar(bar_id, 128);  // row constants ready, scr free
+    // output rows into scr[row][coordinate]: thread i holds coordinate i of O^T
+    {
+      uint32_t o[kRS];
+      if (nchunks > 0) {
+        tmem_ld<kRS>(tmem + lane_q + C::kTO + row0, o);
+        tc_wait_ld();
+      } else {
+#pragma unroll
+        for (int k = 0; k < kRS; ++k) o[k] = 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < kRS; ++k) {
+        const float2 rc = rcs[k];
+        scr[k * 128 + i] = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rc.x, rc.y);
       }
     }
     named_bar(bar_id, 128);
-    // rows row0 + k = n * group + jq, walked incrementally; thread i writes coordinate i
-    int jq = row0 % a.group;
-    float* po = a.part_o + ((((long)(row0 / a.group) * a.B + b) * a.Hq + kvh * a.group + jq) * a.S + split) * kD + i;
-    const long step_j = (long)a.S * kD, step_n = ((long)a.B * a.Hq - a.group) * a.S * kD;
+    // warp sw stores rows sw, sw + 4, ... (512 contiguous bytes each); row
+    // r = n * group + jq is walked without divisions
+    {
+      int n = (row0 + sw) / a.group, jq = (row0 + sw) % a.group;
+      float4 v[kRS / 4];
+      long off[kRS / 4];
 #pragma unroll
-    for (int k = 0; k < kRS; ++k) {
-      if (row0 + k < a.R) *po = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rowc[k], rowc[32 + k]);
-      po += step_j;
-      if (++jq == a.group) {
-        jq = 0;
-        po += step_n;
+      for (int m = 0; m < kRS / 4; ++m) {
+        v[m] = reinterpret_cast<const float4*>(scr + (sw + 4 * m) * 128)[lane];
+        off[m] = ((((long)n * a.B + b) * a.Hq + kvh * a.group + jq) * a.S + split) * kD;
+        jq += 4;
+        while (jq >= a.group) {
+          jq -= a.group;
+          ++n;
+        }
       }
+#pragma unroll
+      for (int m = 0; m < kRS / 4; ++m)
+        if (row0 + sw + 4 * m < a.R) reinterpret_cast<float4*>(a.part_o + off[m])[lane] = v[m];
     }
   }
 
