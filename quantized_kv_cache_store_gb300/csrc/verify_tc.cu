@@ -319,7 +319,9 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
   cta_bar();  // barriers initialised
 
   // the first kStages chunks need no free slot: issue them before the prologue
-  const int prefill = min(nchunks, C::kStages);
+  // only chunk 0 goes out before the prologue: with every CTA streaming its
+  // whole ring at once the first chunk would land last
+  const int prefill = min(nchunks, 1);
   if (warp == 0) {
     for (int c = 0; c < prefill; ++c) {
       if ((c & 3) == 0 && c > 0) fetch_ids(c);
