@@ -161,7 +161,7 @@ def measured_peaks():
 def ncu_traffic(kernel_tag: str, workload: str):
     """Per-launch DRAM bytes of the stage-1 kernel from the committed ncu
     summary, if it was taken on the current kernel source (else None)."""
-    src = os.path.join(ROOT, "quantized_kv_cache_store_gb300", "csrc", "verify.cu")
+    src = os.path.join(ROOT, "quantized_kv_cache_store_gb300", "csrc", "verify_tc.cu")
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}_ncu.txt")
     try:
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
@@ -286,38 +286,37 @@ def bench_workload(name, args, rank, world, pg, dev_props):
 
 
 def per_kernel_durations(sv, stream, G, n_caches):
+    """Average duration of each kernel: a CUDA graph of G launches of that
+    kernel alone (the cache copy rotating as in the step), timed with events
+    on the launching stream after a warm-up replay."""
     import torch
 
-    try:
-        evs = {k: [(torch.cuda.Event(enable_timing=True, external=True),
-                    torch.cuda.Event(enable_timing=True, external=True)) for _ in range(G)]
-               for k in ("tq_store", "tq_verify_stage1", "tq_verify_stage2")}
-    except TypeError:
-        return None
     from quantized_kv_cache_store_gb300 import tqkv
 
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(G):
-            c = i % n_caches
-            a, b = evs["tq_store"][i]
-            a.record(stream)
-            sv.store(c, stream)
-            b.record(stream)
-            a, b = evs["tq_verify_stage1"][i]
-            a.record(stream)
-            tqkv.tq_verify_stage1(sv.caches[c], sv.preset, sv.q, sv.block_table, sv.seq_lens, sv.S,
-                                  sv.wl.causal, sv.part_o, sv.part_lse, stream)
-            b.record(stream)
-            a, b = evs["tq_verify_stage2"][i]
-            a.record(stream)
-            tqkv.tq_verify_stage2(sv.part_o, sv.part_lse, sv.out, stream)
-            b.record(stream)
-    for _ in range(2):
+    calls = {
+        "tq_store": lambda c: sv.store(c, stream),
+        "tq_verify_stage1": lambda c: tqkv.tq_verify_stage1(sv.caches[c], sv.preset, sv.q, sv.block_table,
+                                                            sv.seq_lens, sv.S, sv.wl.causal, sv.part_o,
+                                                            sv.part_lse, stream),
+        "tq_verify_stage2": lambda c: tqkv.tq_verify_stage2(sv.part_o, sv.part_lse, sv.out, stream),
+    }
+    out = {}
+    for name, fn in calls.items():
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(G):
+                fn(i % n_caches)
         with torch.cuda.stream(stream):
             g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(4):
+                g.replay()
+            e1.record(stream)
         torch.cuda.synchronize()
-    return {k: statistics.mean(a.elapsed_time(b) for a, b in v) * 1e3 for k, v in evs.items()}
+        out[name] = e0.elapsed_time(e1) * 1e3 / (4 * G)
+    return out
 
 
 def e2e_measure(res, args):

@@ -182,6 +182,8 @@ __device__ __forceinline__ void store_value4(uint8_t* page, int off, int lane, c
 
 template <int PRESET>
 __global__ void __launch_bounds__(128) store_kernel(StoreArgs a) {
+  pdl_wait();
+  pdl_trigger();
   using L = typename std::conditional<PRESET == 0, K8, K3>::type;
   const int lane = threadIdx.x & 31;
   const long unit = (long)blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -212,11 +214,8 @@ cudaError_t launch_store(int preset, const StoreArgs& a, cudaStream_t st) {
   const long units = (long)a.T * a.Hk;
   if (units == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((units + 3) / 4);
-  if (preset == 0)
-    store_kernel<0><<<grid, 128, 0, st>>>(a);
-  else
-    store_kernel<1><<<grid, 128, 0, st>>>(a);
-  return cudaGetLastError();
+  return preset == 0 ? launch_pdl(store_kernel<0>, dim3(grid), dim3(128), 0, st, a)
+                      : launch_pdl(store_kernel<1>, dim3(grid), dim3(128), 0, st, a);
 }
 
 }  // namespace tq

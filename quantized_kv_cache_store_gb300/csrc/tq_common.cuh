@@ -75,6 +75,28 @@ struct MergeArgs {
   int S;
 };
 
+// Programmatic dependent launch.  Every kernel of the library waits for the
+// previous grid in its stream (and the visibility of its writes) before it
+// touches global memory, and at once allows the next grid to be scheduled, so
+// that launch processing and block dispatch overlap the previous kernel.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Host-side launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_store(int preset, const StoreArgs& a, cudaStream_t st);
 cudaError_t launch_verify_stage1(int preset, const VerifyArgs& a, cudaStream_t st);

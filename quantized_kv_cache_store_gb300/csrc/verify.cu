@@ -98,6 +98,8 @@ struct Smem {
 
 template <int PRESET, int RW, int TW>
 __global__ void __launch_bounds__(RW* TW * 32, 1) verify_stage1_kernel(VerifyArgs a) {
+  pdl_wait();
+  pdl_trigger();
   using L = Layout<PRESET>;
   using RG = Ring<L::kPage, TW>;
   using SM = Smem<PRESET, RW, TW>;
@@ -470,8 +472,12 @@ __global__ void __launch_bounds__(RW* TW * 32, 1) verify_stage1_kernel(VerifyArg
   write_row(rB, mB, lB, zB, 2);
 }
 
-// ---- stage 2: one warp per (n, b, h) row, lane owns 4 coordinates
+// ---- stage 2: one warp per (n, b, h) row, lane owns 4 coordinates; lane s
+// owns split s's weight exp(lse_s - M), broadcast while the partial rows of
+// eight splits are loaded back to back
 __global__ void __launch_bounds__(128) verify_stage2_kernel(MergeArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const long row = (long)blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= a.rows) return;
@@ -481,20 +487,29 @@ __global__ void __launch_bounds__(128) verify_stage2_kernel(MergeArgs a) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
   if (M != -CUDART_INF_F) {
     const float* po = a.part_o + row * a.S * kD + 4 * lane;
-    for (int s = 0; s < a.S; ++s) {
-      const float l = lse[s];
-      if (l == -CUDART_INF_F) continue;
-      const float w = expf(l - M);
-      const float4 v = *reinterpret_cast<const float4*>(po + (long)s * kD);
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
-      den += w;
+    float den = 0.f;
+    for (int s0 = 0; s0 < a.S; s0 += 32) {
+      const int s = s0 + lane;
+      const float l = s < a.S ? lse[s] : -CUDART_INF_F;
+      const float wl = l == -CUDART_INF_F ? 0.f : expf(l - M);
+      den += wl;
+      const int n = min(32, a.S - s0);
+#pragma unroll 8
+      for (int k = 0; k < n; ++k) {
+        const float w = __shfl_sync(kFull, wl, k);
+        const float4 v = *reinterpret_cast<const float4*>(po + (long)(s0 + k) * kD);
+        if (w != 0.f) {  // an empty split contributes nothing
+          acc.x = fmaf(w, v.x, acc.x);
+          acc.y = fmaf(w, v.y, acc.y);
+          acc.z = fmaf(w, v.z, acc.z);
+          acc.w = fmaf(w, v.w, acc.w);
+        }
+      }
     }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
     const float inv = 1.f / den;
     acc.x *= inv;
     acc.y *= inv;
@@ -520,9 +535,7 @@ cudaError_t launch_s1(const VerifyArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  dim3 grid(a.S, a.Hk, a.B);
-  kern<<<grid, RW * TW * 32, SM::kTotal, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(a.S, a.Hk, a.B), dim3(RW * TW * 32), SM::kTotal, st, a);
 }
 
 template <int PRESET>
@@ -544,8 +557,7 @@ cudaError_t launch_verify_stage1(int preset, const VerifyArgs& a, cudaStream_t s
 cudaError_t launch_verify_stage2(const MergeArgs& a, cudaStream_t st) {
   if (a.rows == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((a.rows + 3) / 4);
-  verify_stage2_kernel<<<grid, 128, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(verify_stage2_kernel, dim3(grid), dim3(128), 0, st, a);
 }
 
 }  // namespace tq

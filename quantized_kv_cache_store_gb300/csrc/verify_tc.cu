@@ -244,6 +244,8 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  pdl_wait();
+  pdl_trigger();
 
   // ---- this split's token range
   int L_b = a.seq_lens[b];
@@ -903,9 +905,7 @@ cudaError_t launch_tc(const VerifyArgs& a, cudaStream_t st) {
     e = make_key_map(a, &tmap);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid(a.S, a.Hk, a.B);
-  kern<<<grid, C::kThreads, C::kSmem, st>>>(a, tmap);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(a.S, a.Hk, a.B), dim3(C::kThreads), (size_t)C::kSmem, st, a, tmap);
 }
 
 }  // namespace
