@@ -74,6 +74,46 @@ tq_status check_desc(const tq_cache_desc* d) {
 
 tq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
 
+// validation shared by tq_verify_stage1 and tq_verify; fills the kernel arguments
+tq_status verify_args(const tq_cache_desc* cache, const void* q, const int32_t* block_table, int32_t max_blocks,
+                      const int32_t* seq_lens, int32_t n_spec, int32_t B, int32_t Hq, int32_t num_kv_splits,
+                      int32_t causal, float* partial_o, float* partial_lse, tq::VerifyArgs* out_args) {
+  tq_status s = check_desc(cache);
+  if (s != TQ_OK) return s;
+  if (!q || !block_table || !seq_lens || !partial_o || !partial_lse) return TQ_ERR_INVALID_ARG;
+  if (n_spec < 1 || B < 0 || Hq < 1 || num_kv_splits < 1 || max_blocks < 1) return TQ_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return TQ_ERR_INVALID_ARG;
+  if (Hq % cache->num_kv_heads != 0) return TQ_ERR_INVALID_ARG;
+  const int group = Hq / cache->num_kv_heads;
+  if (n_spec > 16 || n_spec * group > 128) return TQ_ERR_UNSUPPORTED;
+  if (num_kv_splits > 65535 || B > 65535 || max_blocks > (1 << 26)) return TQ_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(partial_o, 16) ||
+      !aligned(partial_lse, 4))
+    return TQ_ERR_MISALIGNED;
+  tq::VerifyArgs& a = *out_args;
+  a.cache = static_cast<const uint8_t*>(cache->cache);
+  a.num_blocks = cache->num_blocks;
+  a.Hk = cache->num_kv_heads;
+  a.q = static_cast<const __half*>(q);
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.seq_lens = seq_lens;
+  a.n_spec = n_spec;
+  a.B = B;
+  a.Hq = Hq;
+  a.group = group;
+  a.R = n_spec * group;
+  a.S = num_kv_splits;
+  a.causal = causal;
+  a.part_o = partial_o;
+  a.part_lse = partial_lse;
+  a.out = nullptr;
+  a.tickets = nullptr;
+  a.csize = 0;
+  a.cb = codebook();
+  return TQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -130,39 +170,34 @@ tq_status tq_verify_stage1(const tq_cache_desc* cache, const void* q, const int3
                            int32_t max_blocks, const int32_t* seq_lens, int32_t n_spec, int32_t B,
                            int32_t Hq, int32_t num_kv_splits, int32_t causal, float* partial_o,
                            float* partial_lse, void* stream) {
-  tq_status s = check_desc(cache);
-  if (s != TQ_OK) return s;
-  if (!q || !block_table || !seq_lens || !partial_o || !partial_lse) return TQ_ERR_INVALID_ARG;
-  if (n_spec < 1 || B < 0 || Hq < 1 || num_kv_splits < 1 || max_blocks < 1) return TQ_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return TQ_ERR_INVALID_ARG;
-  if (Hq % cache->num_kv_heads != 0) return TQ_ERR_INVALID_ARG;
-  const int group = Hq / cache->num_kv_heads;
-  if (n_spec > 16 || n_spec * group > 128) return TQ_ERR_UNSUPPORTED;
-  if (num_kv_splits > 65535 || B > 65535 || max_blocks > (1 << 26)) return TQ_ERR_UNSUPPORTED;
-  if (!aligned(q, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(partial_o, 16) ||
-      !aligned(partial_lse, 4))
-    return TQ_ERR_MISALIGNED;
-  if (B == 0) return TQ_OK;
   tq::VerifyArgs a;
-  a.cache = static_cast<const uint8_t*>(cache->cache);
-  a.num_blocks = cache->num_blocks;
-  a.Hk = cache->num_kv_heads;
-  a.q = static_cast<const __half*>(q);
-  a.block_table = block_table;
-  a.max_blocks = max_blocks;
-  a.seq_lens = seq_lens;
-  a.n_spec = n_spec;
-  a.B = B;
-  a.Hq = Hq;
-  a.group = group;
-  a.R = n_spec * group;
-  a.S = num_kv_splits;
-  a.causal = causal;
-  a.part_o = partial_o;
-  a.part_lse = partial_lse;
-  a.cb = codebook();
+  const tq_status s = verify_args(cache, q, block_table, max_blocks, seq_lens, n_spec, B, Hq, num_kv_splits,
+                                  causal, partial_o, partial_lse, &a);
+  if (s != TQ_OK || B == 0) return s;
   return from_cuda(tq::launch_verify_stage1(cache->preset, a, static_cast<cudaStream_t>(stream)));
 }
+
+tq_status tq_verify(const tq_cache_desc* cache, const void* q, const int32_t* block_table, int32_t max_blocks,
+                    const int32_t* seq_lens, int32_t n_spec, int32_t B, int32_t Hq, int32_t num_kv_splits,
+                    int32_t causal, float* partial_o, float* partial_lse, uint32_t* tickets, float* out,
+                    void* stream) {
+  tq::VerifyArgs a;
+  tq_status s = verify_args(cache, q, block_table, max_blocks, seq_lens, n_spec, B, Hq, num_kv_splits, causal,
+                            partial_o, partial_lse, &a);
+  if (s != TQ_OK) return s;
+  if (!out || !tickets) return TQ_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || !aligned(tickets, 4)) return TQ_ERR_MISALIGNED;
+  if (B == 0) return TQ_OK;
+  a.out = out;
+  a.tickets = tickets;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (tq::verify_fused_supported(cache->preset, a)) return from_cuda(tq::launch_verify_fused(cache->preset, a, st));
+  s = from_cuda(tq::launch_verify_stage1(cache->preset, a, st));
+  if (s != TQ_OK) return s;
+  return tq_verify_stage2(partial_o, partial_lse, n_spec, B, Hq, 128, num_kv_splits, out, stream);
+}
+
+
 
 tq_status tq_verify_stage2(const float* partial_o, const float* partial_lse, int32_t n_spec, int32_t B,
                            int32_t Hq, int32_t head_dim, int32_t num_kv_splits, float* out, void* stream) {

@@ -103,9 +103,9 @@ struct Cfg {
   static constexpr int kP = kQ + align_up(kQBytes, 1024);
   static constexpr int kPBytes = kTok * kLine;  // one buffer
   static constexpr int kCol = kP + 3 * kPBytes;  // float4 [3][128]: score scale, P' scale, v zero, first row
-  // per softmax warpgroup: -m [32], rescale factors [32], row constants [32][2]
+  // per softmax warpgroup: -m [32], rescale factors [32], row constants [32][2], lse [32]
   static constexpr int kRed = kCol + 3 * kTok * 16;
-  static constexpr int kRedWG = 128 * 4;
+  static constexpr int kRedWG = 160 * 4;
   // per softmax warpgroup: float [32 rows][128 tokens or coordinates] for transposes
   static constexpr int kScr = kRed + kSW * kRedWG;
   static constexpr int kScrWG = 32 * 128 * 4;
@@ -225,7 +225,15 @@ __device__ __forceinline__ int kappa(int t) {
   return (t & ~7) | (int)((kPos >> (4 * (t & 7))) & 7u);
 }
 
-template <int PRESET, int NR>
+// FUSED: stage 2 in the same launch.  The S CTAs of a (kv-head, sequence)
+// form S / c thread-block clusters of c CTAs (c = S for S <= 4, S / 2 for
+// S = 6, 8).  CTA q of a cluster merges rows [q R / c, (q + 1) R / c) of the
+// cluster's c splits, reading the peers' normalised rows and log-sum-exps from
+// their shared memory.  With one cluster that is the output; with two, each
+// CTA writes its merged rows as a partial, takes the ticket of its row range,
+// and the CTA that takes the second ticket merges the two partials into the
+// output and sets the ticket back to zero.
+template <int PRESET, int NR, bool FUSED>
 __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     verify_stage1_tc_kernel(VerifyArgs a, const __grid_constant__ CUtensorMap tmap_keys) {
   using C = Cfg<PRESET, NR>;
@@ -797,9 +805,12 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       const float inv = lrow > 0.f ? 1.0f / lrow : 0.f;
       rcs[rr] = make_float2(inv * 16777216.0f, zrow * inv);  // O^T holds codes as fp16 subnormals (code * 2^-24)
       const int row = row0 + rr;
-      if (row < a.R) {
+      const float lse = aborted ? CUDART_NAN_F : (lrow > 0.f ? (-nms[rr] + log2f(lrow)) * kLn2 : -CUDART_INF_F);
+      if constexpr (FUSED) {
+        nms[128 + rr] = lse;
+      } else if (row < a.R) {
         const long orow = (((long)(row / a.group) * a.B + b) * a.Hq + kvh * a.group + row % a.group) * a.S + split;
-        a.part_lse[orow] = aborted ? CUDART_NAN_F : (lrow > 0.f ? (-nms[rr] + log2f(lrow)) * kLn2 : -CUDART_INF_F);
+        a.part_lse[orow] = lse;
       }
     }
     named_bar(bar_id, 128);  // row constants ready, scr free
@@ -822,7 +833,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     named_bar(bar_id, 128);
     // warp sw stores rows sw, sw + 4, ... (512 contiguous bytes each); row
     // r = n * group + jq is walked without divisions
-    {
+    if constexpr (!FUSED) {
       int n = (row0 + sw) / a.group, jq = (row0 + sw) % a.group;
       float4 v[kRS / 4];
       long off[kRS / 4];
@@ -839,6 +850,112 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
 #pragma unroll
       for (int m = 0; m < kRS / 4; ++m)
         if (row0 + sw + 4 * m < a.R) reinterpret_cast<float4*>(a.part_o + off[m])[lane] = v[m];
+    }
+    if constexpr (FUSED) {
+      // ---- stage 2: merge inside the cluster (distributed shared memory),
+      // then, with two clusters, across them through a ticket
+      cluster_sync();  // every CTA of the cluster has staged its rows
+      const int c = a.csize, nclu = a.S / a.csize;
+      const int q = (int)cluster_rank(), g = split / c;
+      const int rpc = (a.R + c - 1) / c, r_lo = q * rpc, r_hi = min(a.R, r_lo + rpc);
+      const int w8 = warp - 8;
+      constexpr int kMW = 4 * C::kSW;  // merging warps (a warp per row)
+      for (int r = r_lo + w8; r < r_hi; r += kMW) {
+        const int jw = r / kRS, kr = r % kRS;
+        const uint32_t lse_at = sbase + C::kRed + jw * C::kRedWG + (128 + kr) * 4;
+        const uint32_t row_at = sbase + C::kScr + jw * C::kScrWG + kr * 512 + 16 * lane;
+        const float l = lane < c ? ld_cluster_f32(map_rank(lse_at, (uint32_t)lane)) : -CUDART_INF_F;
+        float4 v[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) v[t] = t < c ? ld_cluster_v4(map_rank(row_at, (uint32_t)t)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float M = l;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        const float wl = (M == -CUDART_INF_F || l == -CUDART_INF_F) ? 0.f : expf(l - M);
+        float den = wl;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float w = __shfl_sync(kFull, wl, t);
+          if (t < c && w != 0.f) {  // an empty split contributes nothing
+            acc.x = fmaf(w, v[t].x, acc.x);
+            acc.y = fmaf(w, v[t].y, acc.y);
+            acc.z = fmaf(w, v[t].z, acc.z);
+            acc.w = fmaf(w, v[t].w, acc.w);
+          }
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        acc.x *= inv;
+        acc.y *= inv;
+        acc.z *= inv;
+        acc.w *= inv;
+        const long orow = ((long)(r / a.group) * a.B + b) * a.Hq + kvh * a.group + r % a.group;
+        if (nclu == 1) {
+          reinterpret_cast<float4*>(a.out + orow * kD)[lane] = acc;
+        } else {
+          // this cluster's merged row as the partial of split g c
+          reinterpret_cast<float4*>(a.part_o + (orow * a.S + g * c) * kD)[lane] = acc;
+          if (lane == 0) a.part_lse[orow * a.S + g * c] = den > 0.f ? M + logf(den) : (den == 0.f ? -CUDART_INF_F : den);
+        }
+      }
+      if (nclu > 1) {
+        volatile uint32_t* last = reinterpret_cast<volatile uint32_t*>(sm + C::kMisc + 8);
+        uint32_t* ticket = a.tickets + ((long)b * a.Hk + kvh) * 4 + q;
+        named_bar(3, 128 * C::kSW);  // this CTA's merged rows are out
+        if (i == 0 && j == 0) {
+          __threadfence();
+          const uint32_t t = atomicAdd(ticket, 1u);
+          *last = t == (uint32_t)nclu - 1 ? 1u : 0u;
+          if (t == (uint32_t)nclu - 1) *ticket = 0u;  // ready for the next call
+        }
+        named_bar(3, 128 * C::kSW);
+        if (*last) {
+          __threadfence();  // the other cluster's merged rows are visible
+          for (int r = r_lo + w8; r < r_hi; r += kMW) {
+            const long orow = ((long)(r / a.group) * a.B + b) * a.Hq + kvh * a.group + r % a.group;
+            const float l = lane < nclu ? __ldcg(a.part_lse + orow * a.S + lane * c) : -CUDART_INF_F;
+            float4 v[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+              v[t] = t < nclu ? __ldcg(reinterpret_cast<const float4*>(a.part_o + (orow * a.S + t * c) * kD) + lane)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            float M = l;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+            const float wl = (M == -CUDART_INF_F || l == -CUDART_INF_F) ? 0.f : expf(l - M);
+            float den = wl;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const float w = __shfl_sync(kFull, wl, t);
+              if (t < nclu && w != 0.f) {
+                acc.x = fmaf(w, v[t].x, acc.x);
+                acc.y = fmaf(w, v[t].y, acc.y);
+                acc.z = fmaf(w, v[t].z, acc.z);
+                acc.w = fmaf(w, v[t].w, acc.w);
+              }
+            }
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            acc.x *= inv;
+            acc.y *= inv;
+            acc.z *= inv;
+            acc.w *= inv;
+            reinterpret_cast<float4*>(a.out + orow * kD)[lane] = acc;
+          }
+        }
+      }
+      cluster_sync();  // peers may still be reading this CTA's rows
+    }
+  }
+
+  if constexpr (FUSED) {
+    if (warp < 8) {  // the softmax warps pass both inside their merge
+      cluster_sync();
+      cluster_sync();
     }
   }
 
@@ -879,10 +996,10 @@ cudaError_t make_key_map(const VerifyArgs& a, CUtensorMap* m) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int PRESET, int NR>
+template <int PRESET, int NR, bool FUSED>
 cudaError_t launch_tc(const VerifyArgs& a, cudaStream_t st) {
   using C = Cfg<PRESET, NR>;
-  auto kern = verify_stage1_tc_kernel<PRESET, NR>;
+  auto kern = verify_stage1_tc_kernel<PRESET, NR, FUSED>;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -905,7 +1022,53 @@ cudaError_t launch_tc(const VerifyArgs& a, cudaStream_t st) {
     e = make_key_map(a, &tmap);
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(kern, dim3(a.S, a.Hk, a.B), dim3(C::kThreads), (size_t)C::kSmem, st, a, tmap);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.S, a.Hk, a.B);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = FUSED ? (unsigned)a.csize : 1u;
+  attrs[1].val.clusterDim.y = 1;
+  attrs[1].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = FUSED ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, tmap);
+}
+
+// how many clusters of c CTAs of the fused kernel can be resident at once
+template <int PRESET, int NR>
+int fused_capacity(int c) {
+  using C = Cfg<PRESET, NR>;
+  static std::atomic<int> known[16][5];  // per device and cluster size: 0 = not queried, else capacity + 1
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  int v = known[dev & 15][c].load(std::memory_order_acquire);
+  if (v == 0) {
+    auto kern = verify_stage1_tc_kernel<PRESET, NR, true>;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(c, 1, 1);
+      cfg.blockDim = dim3(C::kThreads);
+      cfg.dynamicSmemBytes = C::kSmem;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = (unsigned)c;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();  // a refused query leaves no sticky error
+    v = n + 1;
+    known[dev & 15][c].store(v, std::memory_order_release);
+  }
+  return v - 1;
 }
 
 }  // namespace
@@ -914,13 +1077,38 @@ bool verify_stage1_tc_supported(const VerifyArgs& a) { return a.R <= 64; }
 
 cudaError_t launch_verify_stage1_tc(int preset, const VerifyArgs& a, cudaStream_t st) {
   if (preset == 0) {
-    if (a.R <= 16) return launch_tc<0, 16>(a, st);
-    if (a.R <= 32) return launch_tc<0, 32>(a, st);
-    return launch_tc<0, 64>(a, st);
+    if (a.R <= 16) return launch_tc<0, 16, false>(a, st);
+    if (a.R <= 32) return launch_tc<0, 32, false>(a, st);
+    return launch_tc<0, 64, false>(a, st);
   }
-  if (a.R <= 16) return launch_tc<1, 16>(a, st);
-  if (a.R <= 32) return launch_tc<1, 32>(a, st);
-  return launch_tc<1, 64>(a, st);
+  if (a.R <= 16) return launch_tc<1, 16, false>(a, st);
+  if (a.R <= 32) return launch_tc<1, 32, false>(a, st);
+  return launch_tc<1, 64, false>(a, st);
+}
+
+bool verify_fused_supported(int preset, VerifyArgs& a) {
+  if (a.R > 64) return false;
+  const int c = a.S <= 4 ? a.S : (a.S == 6 || a.S == 8) ? a.S / 2 : 0;
+  if (c < 1) return false;
+  // every cluster resident at once: a wave of clusters would serialise the merge
+  const long clusters = (long)(a.S / c) * a.Hk * a.B;
+  int cap = 0;
+  if (preset == 0) cap = a.R <= 16 ? fused_capacity<0, 16>(c) : a.R <= 32 ? fused_capacity<0, 32>(c) : fused_capacity<0, 64>(c);
+  else cap = a.R <= 16 ? fused_capacity<1, 16>(c) : a.R <= 32 ? fused_capacity<1, 32>(c) : fused_capacity<1, 64>(c);
+  if (clusters > cap) return false;
+  a.csize = c;
+  return true;
+}
+
+cudaError_t launch_verify_fused(int preset, const VerifyArgs& a, cudaStream_t st) {
+  if (preset == 0) {
+    if (a.R <= 16) return launch_tc<0, 16, true>(a, st);
+    if (a.R <= 32) return launch_tc<0, 32, true>(a, st);
+    return launch_tc<0, 64, true>(a, st);
+  }
+  if (a.R <= 16) return launch_tc<1, 16, true>(a, st);
+  if (a.R <= 32) return launch_tc<1, 32, true>(a, st);
+  return launch_tc<1, 64, true>(a, st);
 }
 
 cudaError_t read_device_error(unsigned int* out, bool clear) {

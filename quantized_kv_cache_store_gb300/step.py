@@ -2,7 +2,8 @@
 
 A step is the whole hot path over one batch: ``tq_store`` of the n_spec draft
 tokens of every sequence into the paged cache, then ``tq_verify_stage1`` and
-``tq_verify_stage2``.  Everything is allocated once here (PyTorch device
+``tq_verify_stage2`` (``step``) or the single ``tq_verify`` call
+(``step_fused``).  Everything is allocated once here (PyTorch device
 memory); the calls themselves allocate nothing.
 """
 from __future__ import annotations
@@ -36,6 +37,7 @@ class SpecVerify:
         self.part_o = torch.empty((n, B, Hq, self.S, 128), dtype=torch.float32, device=dev)
         self.part_lse = torch.empty((n, B, Hq, self.S), dtype=torch.float32, device=dev)
         self.out = torch.empty((n, B, Hq, 128), dtype=torch.float32, device=dev)
+        self.tickets = torch.zeros((B, wl.Hk, 4), dtype=torch.int32, device=dev)
 
     def prefill(self, chunk_tokens: int = 1 << 18) -> None:
         """Store the cached prefix of every sequence (untimed set-up)."""
@@ -59,6 +61,18 @@ class SpecVerify:
         tqkv.tq_verify_stage2(self.part_o, self.part_lse, self.out, stream)
         return self.out
 
+    def verify_call(self, i: int = 0, stream=None) -> torch.Tensor:
+        """Both stages through tq_verify (one launch for up to 64 rows per kv-head)."""
+        tqkv.tq_verify(self.caches[i], self.preset, self.q, self.block_table, self.seq_lens, self.S,
+                       self.wl.causal, self.part_o, self.part_lse, self.tickets, self.out, stream)
+        return self.out
+
     def step(self, i: int = 0, stream=None) -> torch.Tensor:
+        """Store the drafts, then stage 1 and stage 2 as two calls."""
         self.store(i, stream)
         return self.verify(i, stream)
+
+    def step_fused(self, i: int = 0, stream=None) -> torch.Tensor:
+        """Store the drafts, then one tq_verify call."""
+        self.store(i, stream)
+        return self.verify_call(i, stream)

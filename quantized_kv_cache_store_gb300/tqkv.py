@@ -75,6 +75,8 @@ def load(build_if_missing: bool = False):
         lib.tq_verify_stage1.argtypes = [D, P, P, I, P, I, I, I, I, I, P, P, P]
         lib.tq_verify_stage2.restype = I
         lib.tq_verify_stage2.argtypes = [P, P, I, I, I, I, I, P, P]
+        lib.tq_verify.restype = I
+        lib.tq_verify.argtypes = [D, P, P, I, P, I, I, I, I, I, P, P, P, P, P]
         lib.tq_device_status.restype = I
         lib.tq_device_status.argtypes = []
         _lib = lib
@@ -183,3 +185,25 @@ def tq_verify_stage2(partial_o: torch.Tensor, partial_lse: torch.Tensor, out: to
                                  _dev(partial_lse, torch.float32, "partial_lse"), n_spec, B, Hq, D, S,
                                  _dev(out, torch.float32, "out"), _stream(stream))
     _check(st, "tq_verify_stage2")
+
+
+def tq_verify(cache: torch.Tensor, preset: int, q: torch.Tensor, block_table: torch.Tensor,
+              seq_lens: torch.Tensor, num_kv_splits: int, causal: bool, partial_o: torch.Tensor,
+              partial_lse: torch.Tensor, tickets: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """Both stages in one call (one launch for up to 64 rows per kv-head).
+    tickets: int32 [B, Hk, 4], zero before the first call, zero again after each."""
+    d = cache_desc(cache, preset)
+    n_spec, B, Hq, D = q.shape
+    S = int(num_kv_splits)
+    if D != 128 or block_table.dim() != 2 or block_table.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("q [n_spec,B,Hq,128], block_table [B,max_blocks], seq_lens [B]")
+    if partial_o.shape != (n_spec, B, Hq, S, 128) or partial_lse.shape != (n_spec, B, Hq, S):
+        raise ValueError("partial_o [n_spec,B,Hq,S,128] and partial_lse [n_spec,B,Hq,S]")
+    if out.shape != (n_spec, B, Hq, 128) or tickets.shape != (B, d.num_kv_heads, 4):
+        raise ValueError("out [n_spec,B,Hq,128], tickets [B,Hk,4]")
+    st = load().tq_verify(ctypes.byref(d), _dev(q, torch.float16, "q"),
+                          _dev(block_table, torch.int32, "block_table"), int(block_table.shape[1]),
+                          _dev(seq_lens, torch.int32, "seq_lens"), n_spec, B, Hq, S, int(bool(causal)),
+                          _dev(partial_o, torch.float32, "partial_o"), _dev(partial_lse, torch.float32, "partial_lse"),
+                          _dev(tickets, torch.int32, "tickets"), _dev(out, torch.float32, "out"), _stream(stream))
+    _check(st, "tq_verify")

@@ -114,3 +114,16 @@ def test_stage2_validation(lib):
     assert s2(D=64) == tqkv.TQ_ERR_UNSUPPORTED
     assert s2(out=FAKE + 4) == tqkv.TQ_ERR_MISALIGNED
     assert s2(pl=FAKE + 2) == tqkv.TQ_ERR_MISALIGNED
+
+
+def test_single_call_validation(lib):
+    d = _desc(ptr=FAKE)
+    v = lambda q=FAKE, t=FAKE, out=FAKE, S=2, B=1: lib.tq_verify(ctypes.byref(d), q, FAKE, 4, FAKE, 8, B, 32, S, 1,
+                                                               FAKE, FAKE, t, out, None)
+    assert v(out=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert v(t=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert v(t=FAKE + 2) == tqkv.TQ_ERR_MISALIGNED
+    assert v(out=FAKE + 4) == tqkv.TQ_ERR_MISALIGNED
+    assert v(q=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert v(S=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert v(B=0) == tqkv.TQ_OK  # nothing to enqueue

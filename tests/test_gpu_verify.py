@@ -241,3 +241,59 @@ def test_unused_slots_with_garbage_do_not_leak():
     out = sv.verify()
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+
+
+# ---- tq_verify: both stages in one call (one launch with a cluster merge for
+# R <= 64 and S in 1..4, 6, 8; else stage 1 + stage 2)
+
+FUSED = [
+    # (preset, n_spec, B, Hq, Hk, seq_len / len_range, S, causal)
+    ("k8v4", 8, 1, 8, 1, 256, 2, True),
+    ("k3v4_nc", 8, 2, 4, 2, 203, 3, False),
+    ("k8v4", 1, 3, 8, 2, (17, 300), 4, True),
+    ("k3v4_nc", 8, 1, 32, 4, 555, 7, True),
+    ("k8v4", 4, 2, 8, 1, 300, 8, True),     # two clusters of four
+    ("k3v4_nc", 4, 2, 6, 3, 40, 1, True),
+    ("k3v4_nc", 8, 2, 16, 2, 900, 6, True),  # two clusters of three
+    ("k8v4", 8, 1, 8, 1, 64, 8, True),      # most splits empty
+    ("k8v4", 3, 2, 2, 2, 3, 5, True),       # splits mostly empty
+    ("k3v4_nc", 2, 1, 16, 1, 77, 16, True),
+    ("k8v4", 2, 3, 8, 4, 700, 40, False),   # more splits than a warp's lanes
+    ("k8v4", 16, 1, 8, 1, 100, 3, True),    # 128 rows: mma.sync stage 1 + stage 2
+]
+
+
+def _fused_run(inp):
+    from quantized_kv_cache_store_gb300.step import SpecVerify
+
+    sv = SpecVerify(inp)
+    sv.prefill()
+    sv.step_fused()
+    torch.cuda.synchronize()
+    fused = sv.out.cpu().numpy()
+    assert not sv.tickets.any()  # left zeroed for the next call
+    sv.verify_call()             # and a second call gives the same result
+    torch.cuda.synchronize()
+    assert np.array_equal(sv.out.cpu().numpy(), fused)
+    sv.verify()
+    torch.cuda.synchronize()
+    return sv.caches[0].cpu().numpy(), fused, sv.out.cpu().numpy()
+
+
+@pytest.mark.parametrize("case", FUSED)
+def test_single_call_verify_matches_oracle(oracle_lib, case):
+    inp = make_inputs(_wl(*case), 77)
+    cache, fused, staged = _fused_run(inp)
+    assert np.array_equal(cache, oracle_cache(oracle_lib, inp))
+    assert_close(fused, _oracle_out(oracle_lib, inp))
+    # same arithmetic as stage 1 + stage 2 up to the order of the merge sums
+    assert_close(fused, staged, atol=1e-5, rtol=1e-5, what="single call vs two calls")
+
+
+@pytest.mark.parametrize("name", ["poc_k8v4", "poc_k3v4_nc"])
+def test_single_call_verify_poc(oracle_lib, name):
+    inp = make_inputs(WORKLOADS[name], 1001)
+    cache, fused, staged = _fused_run(inp)
+    assert_close(fused, _oracle_out(oracle_lib, inp))
+    assert_close(fused, staged, atol=1e-5, rtol=1e-5, what="single call vs two calls")
+    assert tqkv.tq_device_status() == tqkv.TQ_OK
