@@ -108,7 +108,7 @@ struct Cfg {
   static constexpr int kRedWG = 160 * 4;
   // per softmax warpgroup: float [32 rows][128 tokens or coordinates] for transposes
   static constexpr int kScr = kRed + kSW * kRedWG;
-  static constexpr int kScrWG = 32 * 128 * 4;
+  static constexpr int kScrWG = kRS * 128 * 4;
   static constexpr int kPair = kScr + kSW * kScrWG;  // u32 [64][32] (k3v4_nc)
   static constexpr int kPValid = kPair + (PRESET == 1 ? 64 * 32 * 4 : 0);  // u8 [kStages][8]
   static constexpr int kBar = align_up(kPValid + kStages * 8, 8);
@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     float* nms = reinterpret_cast<float*>(sm + C::kRed + j * C::kRedWG);  // -m per row
     float* als = nms + 32;                                                 // rescale factor per row
     float2* rcs = reinterpret_cast<float2*>(nms + 64);                     // (1/l * 2^24, zero term / l)
-    float* scr = reinterpret_cast<float*>(sm + C::kScr + j * C::kScrWG);  // [32][128]
+    float* scr = reinterpret_cast<float*>(sm + C::kScr + j * C::kScrWG);  // [kRS][128]
     // row reductions through scr: thread i sums row rr over tokens [32 qt, 32 qt + 32)
     const int rr = i >> 2, qt = i & 3;
     // this token's line of P' (MN-major, swizzled): byte offsets of its 16-byte chunks
@@ -903,14 +903,14 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       if (nclu > 1) {
         volatile uint32_t* last = reinterpret_cast<volatile uint32_t*>(sm + C::kMisc + 8);
         uint32_t* ticket = a.tickets + ((long)b * a.Hk + kvh) * 4 + q;
-        named_bar(3, 128 * C::kSW);  // this CTA's merged rows are out
+        named_bar(15, 128 * C::kSW);  // this CTA's merged rows are out
         if (i == 0 && j == 0) {
           __threadfence();
           const uint32_t t = atomicAdd(ticket, 1u);
           *last = t == (uint32_t)nclu - 1 ? 1u : 0u;
           if (t == (uint32_t)nclu - 1) *ticket = 0u;  // ready for the next call
         }
-        named_bar(3, 128 * C::kSW);
+        named_bar(15, 128 * C::kSW);
         if (*last) {
           __threadfence();  // the other cluster's merged rows are visible
           for (int r = r_lo + w8; r < r_hi; r += kMW) {
