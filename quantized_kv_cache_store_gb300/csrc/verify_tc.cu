@@ -102,9 +102,9 @@ struct Cfg {
   static constexpr int kQBytes = 2 * NR * 128;  // K-major, 128B swizzle, 2 x 64-coordinate blocks
   static constexpr int kP = kQ + align_up(kQBytes, 1024);
   static constexpr int kPBytes = kTok * kLine;  // one buffer
-  static constexpr int kCol = kP + 3 * kPBytes;  // float4 [3][128]: score scale, P' scale, v zero, first row
+  static constexpr int kCol = kP + 3 * kPBytes;  // float4 [4][128]: score scale, P' scale, v zero, first row
   // per softmax warpgroup: -m [32], rescale factors [32], row constants [32][2], lse [32]
-  static constexpr int kRed = kCol + 3 * kTok * 16;
+  static constexpr int kRed = kCol + 4 * kTok * 16;
   static constexpr int kRedWG = 160 * 4;
   // per softmax warpgroup: float [32 rows][128 tokens or coordinates] for transposes
   static constexpr int kScr = kRed + kSW * kRedWG;
@@ -112,8 +112,8 @@ struct Cfg {
   static constexpr int kPair = kScr + kSW * kScrWG;  // u32 [64][32] (k3v4_nc)
   static constexpr int kPValid = kPair + (PRESET == 1 ? 64 * 32 * 4 : 0);  // u8 [kStages][8]
   static constexpr int kBar = align_up(kPValid + kStages * 8, 8);
-  // full[kStages] empty[kStages] akv[3] qk[2] pfull[3] pv[3]
-  static constexpr int kNumBars = 2 * kStages + 11;
+  // full[kStages] empty[kStages] ak[4] qk[2] pfull[3] pv[3] sfree[2] av[3]
+  static constexpr int kNumBars = 2 * kStages + 17;
   static constexpr int kMisc = kBar + 8 * kNumBars;  // u32 tmem base, u32 abort
   static constexpr int kSmem = kMisc + 16 + 1024;    // + alignment slack
   // tensor memory columns
@@ -126,18 +126,22 @@ struct Cfg {
   static_assert(kSmem <= 227 * 1024, "shared memory overflow");
 };
 
-// Barriers.  Rings indexed by c % 3 (akv, pv) are one deeper than the
-// distance at which they are reused, so that a waiter never sees a barrier
-// two phases ahead of the one it waits for.
+// Barriers.  Each ring is deep enough that no arrival for chunk c + depth can
+// complete before every waiter for chunk c has waited: a waiter never sees a
+// barrier two phases ahead of the one it waits for.  (ak: keys of chunk c + 4
+// need S^T(c + 2) done, issued after softmax(c) released S^T(c), which it
+// does after its own wait on ak(c).)
 struct Bars {
   uint32_t base;
   int stages;
   __device__ uint32_t full(int s) const { return base + 8 * s; }
   __device__ uint32_t empty(int s) const { return base + 8 * (stages + s); }
-  __device__ uint32_t akv(int i) const { return base + 8 * (2 * stages + i); }        // A operands + token params (c % 3)
-  __device__ uint32_t qk(int b) const { return base + 8 * (2 * stages + 3 + b); }     // S^T = K Q^T done (c % 2)
-  __device__ uint32_t pfull(int i) const { return base + 8 * (2 * stages + 5 + i); }  // P' written, S^T read (c % 3)
-  __device__ uint32_t pv(int i) const { return base + 8 * (2 * stages + 8 + i); }     // O^T += V^T P'^T done (c % 3)
+  __device__ uint32_t ak(int i) const { return base + 8 * (2 * stages + i); }         // A_K + token params (c % 4)
+  __device__ uint32_t qk(int b) const { return base + 8 * (2 * stages + 4 + b); }     // S^T = K Q^T done (c % 2)
+  __device__ uint32_t pfull(int i) const { return base + 8 * (2 * stages + 6 + i); }  // P' written (c % 3)
+  __device__ uint32_t pv(int i) const { return base + 8 * (2 * stages + 9 + i); }     // O^T += V^T P'^T done (c % 3)
+  __device__ uint32_t sfree(int b) const { return base + 8 * (2 * stages + 12 + b); } // S^T(c) read by the softmax (c % 2)
+  __device__ uint32_t av(int i) const { return base + 8 * (2 * stages + 14 + i); }    // A_V written (c % 3)
 };
 
 // Bounded wait; false when the CTA aborted or this wait expired (which aborts).
@@ -313,12 +317,16 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       mbar_init(bars.full(s), 1);
       mbar_init(bars.empty(s), 4);
     }
+    for (int i = 0; i < 4; ++i) mbar_init(bars.ak(i), 4);
     for (int i = 0; i < 3; ++i) {
-      mbar_init(bars.akv(i), 4);
+      mbar_init(bars.av(i), 4);
       mbar_init(bars.pv(i), 1);
       mbar_init(bars.pfull(i), 4 * C::kSW);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(bars.qk(i), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars.qk(i), 1);
+      mbar_init(bars.sfree(i), 4 * C::kSW);
+    }
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -425,40 +433,43 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       for (int cc = max(0, c - C::kStages); cc < c; ++cc)
         wait_bar(bars.full(cc % C::kStages), (cc / C::kStages) & 1, abort_flag, false);
     } else if (warp == 1 || warp == 3) {
-      // ================= MMA issuers, one stream each, on two schedulers:
-      // warp 1 issues S^T(c) = K_hat Q^T, warp 3 issues O^T += V^T P'^T
+      // ================= MMA issuers, one thread each.  Warp 1: S^T(c) = K Q^T
+      // once chunk c is dequantised and the softmax has read S^T(c - 2) out of
+      // the same buffer.  Warp 3: O^T += V^T P'^T(c) once the softmax has
+      // written P'(c).  Two threads, so that neither stream waits behind the
+      // other's condition.
       if (lane == 0) {
-        constexpr uint32_t id_qk = idesc_f16(128, NR, 0, 0);
-        constexpr uint32_t id_pv = idesc_f16(128, NR, 0, 1);
-        constexpr uint32_t kQ1 = NR * 8;  // second 64-coordinate block of Q, in 16-byte units
-        constexpr uint32_t kL = C::kLine;  // P' line bytes: 16 lines per K-step
-        int last = -1;
         if (warp == 1) {
+          constexpr uint32_t id_qk = idesc_f16(128, NR, 0, 0);
+          constexpr uint32_t kQ1 = NR * 8;  // second 64-coordinate block of Q, in 16-byte units
           const uint64_t q_desc = smem_desc(sbase + C::kQ, 16, 1024, 2);
-          for (int c = 0; c < nchunks; ++c) {
-            // S^T[c % 2] was read by softmax(c - 2)
-            if (c >= 2 && !wait_bar(bars.pfull((c - 2) % 3), ((c - 2) / 3) & 1, abort_flag)) break;
-            if (!wait_bar(bars.akv(c % 3), (c / 3) & 1, abort_flag)) break;
+          int c = 0;
+          for (; c < nchunks; ++c) {
+            if (c >= 2 && !wait_bar(bars.sfree(c & 1), ((c - 2) >> 1) & 1, abort_flag)) break;
+            if (!wait_bar(bars.ak(c & 3), (c >> 2) & 1, abort_flag)) break;
             tc_fence_after();
             mma_ts_x8<2, 4, 6, kQ1, kQ1 + 2, kQ1 + 4, kQ1 + 6>(tmem + C::kTS + NR * (c & 1),
                                                                tmem + C::kTAK + 64 * (c & 1), q_desc, id_qk, 0u);
             tc_commit(bars.qk(c & 1));
-            last = c;
           }
-          if (last >= 0) wait_bar(bars.qk(last & 1), (last >> 1) & 1, abort_flag, false);
+          // drain before tensor memory is freed
+          if (c > 0) wait_bar(bars.qk((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag, false);
         } else {
+          constexpr uint32_t id_pv = idesc_f16(128, NR, 0, 1);
+          constexpr uint32_t kL = C::kLine;  // P' line bytes: 16 lines per K-step
           const uint64_t p_desc = smem_desc(sbase + C::kP, 16, 8 * C::kLine, C::kSwzMode);
-          for (int c = 0; c < nchunks; ++c) {
-            if (!wait_bar(bars.pfull(c % 3), (c / 3) & 1, abort_flag)) break;
+          int c = 0;
+          for (; c < nchunks; ++c) {
+            if (!wait_bar(bars.pfull(c % 3), (c / 3) & 1, abort_flag) ||
+                !wait_bar(bars.av(c % 3), (c / 3) & 1, abort_flag))
+              break;
             tc_fence_after();
             mma_ts_x8<kL, 2 * kL, 3 * kL, 4 * kL, 5 * kL, 6 * kL, 7 * kL>(
                 tmem + C::kTO, tmem + C::kTAV + 64 * (c % 3), p_desc + (uint64_t)(((c % 3) * C::kPBytes) >> 4), id_pv,
                 c > 0 ? 1u : 0u);
             tc_commit(bars.pv(c % 3));
-            last = c;
           }
-          // drain the MMAs this thread issued before tensor memory is freed
-          if (last >= 0) wait_bar(bars.pv(last % 3), (last / 3) & 1, abort_flag, false);
+          if (c > 0) wait_bar(bars.pv((c - 1) % 3), ((c - 1) / 3) & 1, abort_flag, false);
         }
       }
       __syncwarp();
@@ -470,19 +481,22 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     const int i = tid - 128;
     const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
     const int pg_i = i >> 4, off_i = i & 15;
-    for (int c = 0; c < nchunks; ++c) {
+    // page p's fields of the chunk in ring stage st at pgf(st, p) + L::kVal / kScale / kZero / kNc
+    auto pgf = [&](int st, int p) -> const uint8_t* {
+      const uint8_t* stage = sm + C::kRing + st * C::kStageBytes;
+      return PRESET == 0 ? stage + C::kRestOff + p * C::kRestBytes - C::kKeyBlock : stage + p * L::kPage;
+    };
+    // keys and token parameters of chunk c (run one chunk ahead of the values,
+    // so that S^T(c + 1) never waits behind P.V(c - 2) freeing A_V)
+    auto dq_keys = [&](int c) -> bool {
       const int st = c % C::kStages;
       bool ok = wait_bar(bars.full(st), (c / C::kStages) & 1, abort_flag);
       if (ok && c >= 2) ok = wait_bar(bars.qk(c & 1), ((c - 2) >> 1) & 1, abort_flag);  // A_K[c % 2] read by S^T(c - 2)
-      // A_V[c % 3] and the parameters [c % 3] were read by P.V(c - 3) and softmax(c - 3)
-      if (ok && c >= 3) ok = wait_bar(bars.pv(c % 3), ((c - 3) / 3) & 1, abort_flag);
+      // parameters [c % 4] were read by softmax(c - 4), which released S^T(c - 4)
+      // before S^T(c - 2) was issued
       __syncwarp();
-      if (!ok) break;
+      if (!ok) return false;
       const uint8_t* stage = sm + C::kRing + st * C::kStageBytes;
-      // page p's fields at pgf(p) + L::kVal / kScale / kZero / kNc
-      auto pgf = [&](int p) -> const uint8_t* {
-        return PRESET == 0 ? stage + C::kRestOff + p * C::kRestBytes - C::kKeyBlock : stage + p * L::kPage;
-      };
       // keys of token i, all 128 coordinates -> A_K[c % 2]
       const uint32_t ak = tmem + lane_q + C::kTAK + 64 * (c & 1);
       if constexpr (PRESET == 0) {
@@ -531,27 +545,6 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
           tmem_st32(ak + 32 * h, r);
         }
       }
-      // value codes of coordinate i, all 128 tokens -> A_V[c % 3]: word x of
-      // eight codes (token k in bits 4k .. 4k+3) gives the columns
-      // (t0, 16 t5) (16 t1, t4) (t2, 16 t7) (16 t3, t6) of its group of 8
-      const uint32_t av = tmem + lane_q + C::kTAV + 64 * (c % 3);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t r[32];
-#pragma unroll
-        for (int pp = 0; pp < 4; ++pp) {
-          const uint2 w = *reinterpret_cast<const uint2*>(pgf(4 * h + pp) + L::kVal + 8 * i);
-#pragma unroll
-          for (int hw = 0; hw < 2; ++hw) {
-            const uint32_t x = hw ? w.y : w.x, x8 = x >> 8;
-            r[8 * pp + 4 * hw + 0] = x & 0x00F0000Fu;
-            r[8 * pp + 4 * hw + 1] = x & 0x000F00F0u;
-            r[8 * pp + 4 * hw + 2] = x8 & 0x00F0000Fu;
-            r[8 * pp + 4 * hw + 3] = x8 & 0x000F00F0u;
-          }
-        }
-        tmem_st32(av + 32 * h, r);
-      }
       // per-token parameters of token i
       {
         const int pos = (page_lo + c * C::kPages) * kBlock + i;
@@ -559,7 +552,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         float cs = sl2, sv = 0.f, zv = 0.f;
         int rmin = 1 << 20;
         if (valid) {
-          const uint8_t* pg = pgf(pg_i);
+          const uint8_t* pg = pgf(st, pg_i);
           if constexpr (PRESET == 1)
             cs = __half2float(*reinterpret_cast<const __half*>(pg + L::kNc + 2 * off_i)) * sl2;
           // odd tokens enter the value operand 16 times larger
@@ -571,15 +564,55 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
             rmin = nmin <= 0 ? 0 : nmin * a.group;
           }
         }
-        colp[(c % 3) * 128 + i] = make_float4(cs, sv, zv, __int_as_float(rmin));
+        colp[(c & 3) * 128 + i] = make_float4(cs, sv, zv, __int_as_float(rmin));
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.ak(c & 3));
+      return true;
+    };
+    // values of chunk c; then its ring stage is free
+    auto dq_values = [&](int c) -> bool {
+      const int st = c % C::kStages;
+      // A_V[c % 3] was read by P.V(c - 3)
+      const bool ok = c < 3 || wait_bar(bars.pv(c % 3), ((c - 3) / 3) & 1, abort_flag);
+      __syncwarp();
+      if (!ok) return false;
+      // value codes of coordinate i, all 128 tokens -> A_V[c % 3]: word x of
+      // eight codes (token k in bits 4k .. 4k+3) gives the columns
+      // (t0, 16 t5) (16 t1, t4) (t2, 16 t7) (16 t3, t6) of its group of 8
+      const uint32_t av = tmem + lane_q + C::kTAV + 64 * (c % 3);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[32];
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+          const uint2 w = *reinterpret_cast<const uint2*>(pgf(st, 4 * h + pp) + L::kVal + 8 * i);
+#pragma unroll
+          for (int hw = 0; hw < 2; ++hw) {
+            const uint32_t x = hw ? w.y : w.x, x8 = x >> 8;
+            r[8 * pp + 4 * hw + 0] = x & 0x00F0000Fu;
+            r[8 * pp + 4 * hw + 1] = x & 0x000F00F0u;
+            r[8 * pp + 4 * hw + 2] = x8 & 0x00F0000Fu;
+            r[8 * pp + 4 * hw + 3] = x8 & 0x000F00F0u;
+          }
+        }
+        tmem_st32(av + 32 * h, r);
       }
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bars.akv(c % 3));
+        mbar_arrive(bars.av(c % 3));
         mbar_arrive(bars.empty(st));
       }
+      return true;
+    };
+    bool ok = nchunks == 0 || dq_keys(0);
+    for (int c = 0; c < nchunks && ok; ++c) {
+      if (c + 1 < nchunks) ok = dq_keys(c + 1);
+      ok = ok && dq_values(c);
     }
   } else {
     regs_inc<C::kRegSm>();
@@ -627,14 +660,14 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     for (int c = 0; c < nchunks; ++c) {
       bool ok = !aborted;
       if (!pre) {
-        ok = ok && wait_bar(bars.akv(c % 3), (c / 3) & 1, abort_flag) &&
+        ok = ok && wait_bar(bars.ak(c & 3), (c >> 2) & 1, abort_flag) &&
              wait_bar(bars.qk(c & 1), (c >> 1) & 1, abort_flag);
         __syncwarp();
         tc_fence_after();
         tmem_ld<kRS>(s_base + NR * (c & 1), x);
       }
       tc_wait_ld();
-      const float4 cp = colp[(c % 3) * 128 + i];
+      const float4 cp = colp[(c & 3) * 128 + i];
       const int rmin = __float_as_int(cp.w);
       const bool masked = __any_sync(kFull, rmin > row0);
       float2* d = reinterpret_cast<float2*>(x);
@@ -666,16 +699,24 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         if (k + 1 < kH) mx1 = fmax3(mx1, d[k + 1].x, d[k + 1].y);
       }
       // leave the loop together: the named barriers need all four warps
+      // S^T(c) is released to the MMA issuer (for S^T(c + 2)) once no path of
+      // this chunk reads it again
+      auto release_s = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.sfree(c & 1));
+      };
       if (bar_red_or(bar_id, 128, fmaxf(mx0, mx1) > kRescaleThreshold || !ok)) {
         if (bar_red_or(bar_id, 128, !ok)) {
           aborted = true;
           break;
         }
         // exact maximum of this chunk for each row over the 128 tokens: the
-        // raw scaled scores (S^T(c) stays valid until this chunk's pfull) are
-        // transposed through scr and reduced per row
+        // raw scaled scores (S^T(c) is still held) are transposed through scr
+        // and reduced per row
         tmem_ld<kRS>(s_base + NR * (c & 1), x);
         tc_wait_ld();
+        release_s();
 #pragma unroll
         for (int k = 0; k < kRS; ++k)
           scr[tr_index(k, i)] = (masked && row0 + k < rmin) ? -CUDART_INF_F : __uint_as_float(x[k]) * cp.x;
@@ -730,6 +771,8 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
           tc_wait_st();
         }
         scores();
+      } else {
+        release_s();
       }
       // probabilities, row sums, zero term; P' = p * scale into the MN-major B tile
       uint32_t pk[kH];
@@ -747,7 +790,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       pre = false;
       if (c + 1 < nchunks) {
         const int cn = c + 1;
-        const bool rdy = mbar_test_wait(bars.akv(cn % 3), (cn / 3) & 1) && mbar_test_wait(bars.qk(cn & 1), (cn >> 1) & 1);
+        const bool rdy = mbar_test_wait(bars.ak(cn & 3), (cn >> 2) & 1) && mbar_test_wait(bars.qk(cn & 1), (cn >> 1) & 1);
         if (__all_sync(kFull, rdy)) {
           tc_fence_after();
           tmem_ld<kRS>(s_base + NR * (cn & 1), x);
