@@ -159,21 +159,24 @@ tq_status tq_verify_stage2(const float* partial_o, const float* partial_lse, int
  * query head, as tq_verify_stage1 followed by tq_verify_stage2 (the
  * split-KV partial attention, "sycl-three-attempts-arc-b70" section "Part 3",
  * and its log-sum-exp merge).  The pages run the two stages as two launches.
- * Here, when n_spec * Hq / Hk <= 64, num_kv_splits is 1..4, 6 or 8 and every
- * thread-block cluster can be resident at once, one launch runs both: the S
- * CTAs of a (kv-head, sequence) form S / c clusters of c CTAs (c = S up to 4,
- * else S / 2) that merge their rows through distributed shared memory; with
- * two clusters each writes its merged rows as a partial and the second to
- * take the ticket of a row range merges the two.  Otherwise stage 1 and stage
- * 2 are enqueued as two launches.
+ * Here, when n_spec * Hq / Hk <= 64, num_kv_splits <= 32 and all
+ * num_kv_splits * Hk * B CTAs fit on the device at once, one cooperative
+ * launch runs both: every split writes its partial rows, counts itself in
+ * on a per-(sequence, kv-head) counter, waits (bounded) until all splits of
+ * that pair have, then merges its share of the rows (split s: rows
+ * [s r, (s + 1) r), r = ceil(R / S)).  Otherwise stage 1 and stage 2 are
+ * enqueued as two launches.
  * Arguments, layouts, alignment and validation are those of
  * tq_verify_stage1 (its first twelve arguments; the partials are scratch
- * here) plus
+ * here and their contents unspecified afterwards) plus
  *   tickets  u32 [B][Hk][4], 4-byte aligned, caller-owned: must be all zero
  *            before the first call and is all zero again after each call
- *            completes; calls that share a tickets buffer must not overlap in
- *            time (order them on one stream);
- *   out      fp32 [n_spec][B][Hq][128], 16-byte aligned; written. */
+ *            completes (entries 0 and 1 of each pair are its arrival and
+ *            completion counters); calls that share a tickets buffer must not
+ *            overlap in time (order them on one stream);
+ *   out      fp32 [n_spec][B][Hq][128], 16-byte aligned; written.
+ * A cross-split wait that expires writes NaN rows and sets the device error
+ * word (tq_device_status). */
 tq_status tq_verify(const tq_cache_desc* cache, const void* q, const int32_t* block_table,
                     int32_t max_blocks, const int32_t* seq_lens, int32_t n_spec, int32_t B,
                     int32_t Hq, int32_t num_kv_splits, int32_t causal, float* partial_o,

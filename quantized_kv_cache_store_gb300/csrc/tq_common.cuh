@@ -66,7 +66,6 @@ struct VerifyArgs {
   float* part_lse;
   float* out;         // merged output (single-launch verify only)
   uint32_t* tickets;  // [B][Hk][4], zero between calls (single-launch verify only)
-  int csize;          // CTAs per cluster (single-launch verify only)
   Codebook cb;
 };
 
@@ -107,9 +106,9 @@ cudaError_t launch_verify_stage2(const MergeArgs& a, cudaStream_t st);
 // tensor-core stage 1 (tcgen05), used for up to 64 query rows per kv-head
 bool verify_stage1_tc_supported(const VerifyArgs& a);
 cudaError_t launch_verify_stage1_tc(int preset, const VerifyArgs& a, cudaStream_t st);
-// both stages in one launch (up to 64 rows per kv-head, S in 1..4, 6 or 8):
-// fills a.csize when supported
-bool verify_fused_supported(int preset, VerifyArgs& a);
+// both stages in one cooperative launch (up to 64 rows per kv-head, S <= 32,
+// every CTA resident at once)
+bool verify_fused_supported(int preset, const VerifyArgs& a);
 cudaError_t launch_verify_fused(int preset, const VerifyArgs& a, cudaStream_t st);
 // sticky device-side error word (nonzero after a bounded wait expired)
 cudaError_t read_device_error(unsigned int* out, bool clear);

@@ -109,7 +109,6 @@ tq_status verify_args(const tq_cache_desc* cache, const void* q, const int32_t* 
   a.part_lse = partial_lse;
   a.out = nullptr;
   a.tickets = nullptr;
-  a.csize = 0;
   a.cb = codebook();
   return TQ_OK;
 }

@@ -67,6 +67,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 // a bounded wait gives up after kWaitTries tests of up to kSuspendNs each (~1 s)
 constexpr uint32_t kWaitTries = 50000;
 constexpr uint32_t kSuspendNs = 20000;
+// the cross-CTA wait of the single-launch verify gives up after kSpinTries
+// polls (a poll is an L2 round trip plus a 64 ns sleep: well over 100 ms)
+constexpr uint32_t kSpinTries = 1u << 20;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -112,7 +115,8 @@ struct Cfg {
   static constexpr int kPair = kScr + kSW * kScrWG;  // u32 [64][32] (k3v4_nc)
   static constexpr int kPValid = kPair + (PRESET == 1 ? 64 * 32 * 4 : 0);  // u8 [kStages][8]
   static constexpr int kBar = align_up(kPValid + kStages * 8, 8);
-  // full[kStages] empty[kStages] ak[4] qk[2] pfull[3] pv[3] sfree[2] av[3]
+  // full[kStages] empty[kStages] ak[4] sready[2] pfull[3] pv[3] sfree[2] av[3]
+  static constexpr int kProducers = 3;  // warps 0, 2, 3 copy pages 0-2, 3-5, 6-7 of a chunk
   static constexpr int kNumBars = 2 * kStages + 17;
   static constexpr int kMisc = kBar + 8 * kNumBars;  // u32 tmem base, u32 abort
   static constexpr int kSmem = kMisc + 16 + 1024;    // + alignment slack
@@ -137,12 +141,28 @@ struct Bars {
   __device__ uint32_t full(int s) const { return base + 8 * s; }
   __device__ uint32_t empty(int s) const { return base + 8 * (stages + s); }
   __device__ uint32_t ak(int i) const { return base + 8 * (2 * stages + i); }         // A_K + token params (c % 4)
-  __device__ uint32_t qk(int b) const { return base + 8 * (2 * stages + 4 + b); }     // S^T = K Q^T done (c % 2)
+  // S^T = K Q^T done and chunk c's parameters written (c % 2): four dequant
+  // arrivals plus the issuer's commit, which also covers every earlier P.V
+  __device__ uint32_t sready(int b) const { return base + 8 * (2 * stages + 4 + b); }
   __device__ uint32_t pfull(int i) const { return base + 8 * (2 * stages + 6 + i); }  // P' written (c % 3)
   __device__ uint32_t pv(int i) const { return base + 8 * (2 * stages + 9 + i); }     // O^T += V^T P'^T done (c % 3)
   __device__ uint32_t sfree(int b) const { return base + 8 * (2 * stages + 12 + b); } // S^T(c) read by the softmax (c % 2)
   __device__ uint32_t av(int i) const { return base + 8 * (2 * stages + 14 + i); }    // A_V written (c % 3)
 };
+
+// Bounded wait for a global counter written by other CTAs of the same
+// (cooperative, hence co-resident) grid to reach target; false when it
+// expired, which is recorded in the device error word.
+__device__ __forceinline__ bool spin_until_at_least(const uint32_t* counter, uint32_t target) {
+  for (uint32_t i = 0; i < kSpinTries; ++i) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+    if (v >= target) return true;
+    __nanosleep(64);
+  }
+  atomicOr(&g_tq_device_error, 1u);
+  return false;
+}
 
 // Bounded wait; false when the CTA aborted or this wait expired (which aborts).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
@@ -229,14 +249,12 @@ __device__ __forceinline__ int kappa(int t) {
   return (t & ~7) | (int)((kPos >> (4 * (t & 7))) & 7u);
 }
 
-// FUSED: stage 2 in the same launch.  The S CTAs of a (kv-head, sequence)
-// form S / c thread-block clusters of c CTAs (c = S for S <= 4, S / 2 for
-// S = 6, 8).  CTA q of a cluster merges rows [q R / c, (q + 1) R / c) of the
-// cluster's c splits, reading the peers' normalised rows and log-sum-exps from
-// their shared memory.  With one cluster that is the output; with two, each
-// CTA writes its merged rows as a partial, takes the ticket of its row range,
-// and the CTA that takes the second ticket merges the two partials into the
-// output and sets the ticket back to zero.
+// FUSED: stage 2 in the same launch, a cooperative grid (every CTA
+// resident).  The S splits of a (sequence, kv-head) write their partial rows
+// into the scratch partials ([B][Hk][S][R] layout, a CTA's rows contiguous),
+// count themselves in on the pair's arrival counter and wait for all S; split
+// s then merges rows [s r, (s + 1) r) (r = ceil(R / S)) into the output.  The
+// last split to finish its merge sets both counters back to zero.
 template <int PRESET, int NR, bool FUSED>
 __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     verify_stage1_tc_kernel(VerifyArgs a, const __grid_constant__ CUtensorMap tmap_keys) {
@@ -271,50 +289,56 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
   const int nchunks = (npages + C::kPages - 1) / C::kPages;
   const int32_t* bt = a.block_table + (long)b * a.max_blocks;
 
-  // Producer = warp 0 (all lanes wait together; lane 0 issues the copies).
-  // Block ids are fetched 32 pages (4 chunks) at a time, one id per lane.
-  int ids = -1;  // this lane's block id for page 32 * (c / 4) + lane
-  auto fetch_ids = [&](int c) {
+  // Producers = warps 0, 2, 3 (C::kProducers): producer w copies pages
+  // [3 w, 3 w + 3) of each chunk, one page per lane, since a warp issues its
+  // lanes' copies one after another and each costs tens of cycles.  Block ids
+  // are fetched 32 pages (4 chunks) at a time, one id per lane, a group ahead.
+  const bool producer = warp == 0 || warp == 2 || warp == 3;
+  const int pw = warp == 0 ? 0 : warp - 1;
+  const int p_lo = 3 * pw, p_hi = min(C::kPages, p_lo + 3);
+  int ids = -1, ids_next = -1;  // this lane's block id for page 32 * (c / 4) + lane, and for the next group
+  auto fetch_ids = [&](int c) -> int {
     const int lp = c * C::kPages + lane;
-    ids = -1;
+    int id = -1;
     if (lp < npages) {
-      const int id = bt[page_lo + lp];
-      ids = (id >= 0 && id < a.num_blocks) ? id : -1;
+      id = bt[page_lo + lp];
+      id = (id >= 0 && id < a.num_blocks) ? id : -1;
     }
+    return id;
   };
   auto produce = [&](int c) {
     const int st = c % C::kStages;
     const int mine = __shfl_sync(kFull, ids, (c & 3) * C::kPages + (lane & 7));
-    const uint32_t nvalid = __popc(__ballot_sync(kFull, lane < C::kPages && mine >= 0));
-    const uint32_t bytes = nvalid * (uint32_t)L::kPage;
+    const bool my = lane >= p_lo && lane < p_hi;
+    const uint32_t nvalid = __popc(__ballot_sync(kFull, my && mine >= 0));
     // page flags first: the arrive below releases them to the consumers
-    if (lane < C::kPages) pvalid[st * 8 + lane] = mine >= 0 ? 1 : 0;
+    if (my) pvalid[st * 8 + lane] = mine >= 0 ? 1 : 0;
     __syncwarp();
-    if (lane == 0) mbar_arrive_expect_tx(bars.full(st), bytes);
+    if (lane == 0) mbar_arrive_expect_tx(bars.full(st), nvalid * (uint32_t)L::kPage);
     __syncwarp();
-    // lane p issues page p's copies (one issuing thread would serialise them)
-    if (lane < C::kPages) {
-      const int id = mine;
-      if (id >= 0) {
-        const uint32_t dst = sbase + C::kRing + st * C::kStageBytes;
-        const long page = (long)id * a.Hk + kvh;
-        const uint8_t* src = a.cache + page * L::kPage;
-        if constexpr (PRESET == 0) {
-          tma_load_3d(dst + lane * C::kKeyBlock, &tmap_keys, 0, 0, (int)page, bars.full(st));
-          bulk_g2s(dst + C::kRestOff + lane * C::kRestBytes, src + C::kKeyBlock, C::kRestBytes, bars.full(st));
-        } else {
-          bulk_g2s(dst + lane * L::kPage, src, L::kPage, bars.full(st));
-        }
+    if (my && mine >= 0) {
+      const uint32_t dst = sbase + C::kRing + st * C::kStageBytes;
+      const long page = (long)mine * a.Hk + kvh;
+      const uint8_t* src = a.cache + page * L::kPage;
+      if constexpr (PRESET == 0) {
+        tma_load_3d(dst + lane * C::kKeyBlock, &tmap_keys, 0, 0, (int)page, bars.full(st));
+        bulk_g2s(dst + C::kRestOff + lane * C::kRestBytes, src + C::kKeyBlock, C::kRestBytes, bars.full(st));
+      } else {
+        bulk_g2s(dst + lane * L::kPage, src, L::kPage, bars.full(st));
       }
     }
     __syncwarp();
   };
-  if (warp == 0 && nchunks > 0) fetch_ids(0);  // in flight during the set-up
+  if (producer && nchunks > 0) {  // in flight during the set-up
+    if (PRESET == 0 && lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_keys) : "memory");
+    ids = fetch_ids(0);
+    ids_next = fetch_ids(4);
+  }
 
   // ---- set-up: barriers, tensor memory
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bars.full(s), 1);
+      mbar_init(bars.full(s), C::kProducers);
       mbar_init(bars.empty(s), 4);
     }
     for (int i = 0; i < 4; ++i) mbar_init(bars.ak(i), 4);
@@ -324,7 +348,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       mbar_init(bars.pfull(i), 4 * C::kSW);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bars.qk(i), 1);
+      mbar_init(bars.sready(i), 5);
       mbar_init(bars.sfree(i), 4 * C::kSW);
     }
     *abort_flag = 0u;
@@ -340,12 +364,8 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
   // only chunk 0 goes out before the prologue: with every CTA streaming its
   // whole ring at once the first chunk would land last
   const int prefill = min(nchunks, 1);
-  if (warp == 0) {
-    for (int c = 0; c < prefill; ++c) {
-      if ((c & 3) == 0 && c > 0) fetch_ids(c);
-      produce(c);
-    }
-  }
+  if (producer)
+    for (int c = 0; c < prefill; ++c) produce(c);
 
   // ---- query rows (dequant + softmax warpgroups) and code-pair table (warps 2-3)
   if (tid >= 128) {
@@ -421,56 +441,66 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
 
   if (warp < 4) {
     regs_dec<C::kRegCtl>();
-    if (warp == 0) {
-      // ================= producer: 8 pages per chunk into the ring
+    if (producer) {
+      // ================= producers: their pages of each chunk into the ring
       int c = prefill;
       for (; c < nchunks; ++c) {
-        if ((c & 3) == 0) fetch_ids(c);
+        if ((c & 3) == 0) {
+          ids = ids_next;
+          ids_next = fetch_ids(c + 4);  // lands while this group is copied
+        }
         if (!wait_bar(bars.empty(c % C::kStages), ((c / C::kStages) - 1) & 1, abort_flag)) break;
         produce(c);
       }
       // drain: copies still in flight must land before the CTA can exit
       for (int cc = max(0, c - C::kStages); cc < c; ++cc)
         wait_bar(bars.full(cc % C::kStages), (cc / C::kStages) & 1, abort_flag, false);
-    } else if (warp == 1 || warp == 3) {
-      // ================= MMA issuers, one thread each.  Warp 1: S^T(c) = K Q^T
-      // once chunk c is dequantised and the softmax has read S^T(c - 2) out of
-      // the same buffer.  Warp 3: O^T += V^T P'^T(c) once the softmax has
-      // written P'(c).  Two threads, so that neither stream waits behind the
-      // other's condition.
+    } else if (warp == 1) {
+      // ================= MMA issuer (one thread), in the order P.V(c - 3),
+      // S^T(c): P.V(c - 3) waits for softmax(c - 3), S^T(c) for softmax(c - 2)
+      // to release its buffer, so neither waits behind the other.  Since a
+      // commit tracks every earlier MMA of this thread, sready(c) also means
+      // that P.V(c - 3) is done: P' buffer c % 3 and A_V buffer c % 3 are free.
       if (lane == 0) {
-        if (warp == 1) {
-          constexpr uint32_t id_qk = idesc_f16(128, NR, 0, 0);
-          constexpr uint32_t kQ1 = NR * 8;  // second 64-coordinate block of Q, in 16-byte units
-          const uint64_t q_desc = smem_desc(sbase + C::kQ, 16, 1024, 2);
-          int c = 0;
-          for (; c < nchunks; ++c) {
-            if (c >= 2 && !wait_bar(bars.sfree(c & 1), ((c - 2) >> 1) & 1, abort_flag)) break;
-            if (!wait_bar(bars.ak(c & 3), (c >> 2) & 1, abort_flag)) break;
-            tc_fence_after();
-            mma_ts_x8<2, 4, 6, kQ1, kQ1 + 2, kQ1 + 4, kQ1 + 6>(tmem + C::kTS + NR * (c & 1),
-                                                               tmem + C::kTAK + 64 * (c & 1), q_desc, id_qk, 0u);
-            tc_commit(bars.qk(c & 1));
+        constexpr uint32_t id_qk = idesc_f16(128, NR, 0, 0);
+        constexpr uint32_t id_pv = idesc_f16(128, NR, 0, 1);
+        constexpr uint32_t kQ1 = NR * 8;  // second 64-coordinate block of Q, in 16-byte units
+        constexpr uint32_t kL = C::kLine;  // P' line bytes: 16 lines per K-step
+        const uint64_t q_desc = smem_desc(sbase + C::kQ, 16, 1024, 2);
+        const uint64_t p_desc = smem_desc(sbase + C::kP, 16, 8 * C::kLine, C::kSwzMode);
+        auto issue_qk = [&](int c) -> bool {
+          if (c >= 2 && !wait_bar(bars.sfree(c & 1), ((c - 2) >> 1) & 1, abort_flag)) return false;
+          if (!wait_bar(bars.ak(c & 3), (c >> 2) & 1, abort_flag)) return false;
+          tc_fence_after();
+          mma_ts_x8<2, 4, 6, kQ1, kQ1 + 2, kQ1 + 4, kQ1 + 6>(tmem + C::kTS + NR * (c & 1), tmem + C::kTAK + 64 * (c & 1),
+                                                             q_desc, id_qk, 0u);
+          tc_commit(bars.sready(c & 1));
+          return true;
+        };
+        auto issue_pv = [&](int c) -> bool {
+          if (!wait_bar(bars.pfull(c % 3), (c / 3) & 1, abort_flag) || !wait_bar(bars.av(c % 3), (c / 3) & 1, abort_flag))
+            return false;
+          tc_fence_after();
+          mma_ts_x8<kL, 2 * kL, 3 * kL, 4 * kL, 5 * kL, 6 * kL, 7 * kL>(
+              tmem + C::kTO, tmem + C::kTAV + 64 * (c % 3), p_desc + (uint64_t)(((c % 3) * C::kPBytes) >> 4), id_pv,
+              c > 0 ? 1u : 0u);
+          tc_commit(bars.pv(c % 3));
+          return true;
+        };
+        int done_qk = 0, done_pv = 0;
+        for (int c = 0; c < nchunks + 3; ++c) {
+          if (c >= 3) {
+            if (!issue_pv(c - 3)) break;
+            ++done_pv;
           }
-          // drain before tensor memory is freed
-          if (c > 0) wait_bar(bars.qk((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag, false);
-        } else {
-          constexpr uint32_t id_pv = idesc_f16(128, NR, 0, 1);
-          constexpr uint32_t kL = C::kLine;  // P' line bytes: 16 lines per K-step
-          const uint64_t p_desc = smem_desc(sbase + C::kP, 16, 8 * C::kLine, C::kSwzMode);
-          int c = 0;
-          for (; c < nchunks; ++c) {
-            if (!wait_bar(bars.pfull(c % 3), (c / 3) & 1, abort_flag) ||
-                !wait_bar(bars.av(c % 3), (c / 3) & 1, abort_flag))
-              break;
-            tc_fence_after();
-            mma_ts_x8<kL, 2 * kL, 3 * kL, 4 * kL, 5 * kL, 6 * kL, 7 * kL>(
-                tmem + C::kTO, tmem + C::kTAV + 64 * (c % 3), p_desc + (uint64_t)(((c % 3) * C::kPBytes) >> 4), id_pv,
-                c > 0 ? 1u : 0u);
-            tc_commit(bars.pv(c % 3));
+          if (c < nchunks) {
+            if (!issue_qk(c)) break;
+            ++done_qk;
           }
-          if (c > 0) wait_bar(bars.pv((c - 1) % 3), ((c - 1) / 3) & 1, abort_flag, false);
         }
+        // drain before tensor memory is freed
+        if (done_qk > 0) wait_bar(bars.sready((done_qk - 1) & 1), ((done_qk - 1) >> 1) & 1, abort_flag, false);
+        if (done_pv > 0) wait_bar(bars.pv((done_pv - 1) % 3), ((done_pv - 1) / 3) & 1, abort_flag, false);
       }
       __syncwarp();
     }
@@ -491,7 +521,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     auto dq_keys = [&](int c) -> bool {
       const int st = c % C::kStages;
       bool ok = wait_bar(bars.full(st), (c / C::kStages) & 1, abort_flag);
-      if (ok && c >= 2) ok = wait_bar(bars.qk(c & 1), ((c - 2) >> 1) & 1, abort_flag);  // A_K[c % 2] read by S^T(c - 2)
+      if (ok && c >= 2) ok = wait_bar(bars.sready(c & 1), ((c - 2) >> 1) & 1, abort_flag);  // A_K[c % 2] read by S^T(c - 2)
       // parameters [c % 4] were read by softmax(c - 4), which released S^T(c - 4)
       // before S^T(c - 2) was issued
       __syncwarp();
@@ -569,14 +599,18 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars.ak(c & 3));
+      if (lane == 0) {
+        mbar_arrive(bars.ak(c & 3));
+        mbar_arrive(bars.sready(c & 1));
+      }
       return true;
     };
     // values of chunk c; then its ring stage is free
     auto dq_values = [&](int c) -> bool {
       const int st = c % C::kStages;
-      // A_V[c % 3] was read by P.V(c - 3)
-      const bool ok = c < 3 || wait_bar(bars.pv(c % 3), ((c - 3) / 3) & 1, abort_flag);
+      // A_V[c % 3] was read by P.V(c - 3), done once sready(c) is (the keys of
+      // chunk c, already dequantised, are its only other condition)
+      const bool ok = c < 3 || wait_bar(bars.sready(c & 1), (c >> 1) & 1, abort_flag);
       __syncwarp();
       if (!ok) return false;
       // value codes of coordinate i, all 128 tokens -> A_V[c % 3]: word x of
@@ -660,8 +694,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     for (int c = 0; c < nchunks; ++c) {
       bool ok = !aborted;
       if (!pre) {
-        ok = ok && wait_bar(bars.ak(c & 3), (c >> 2) & 1, abort_flag) &&
-             wait_bar(bars.qk(c & 1), (c >> 1) & 1, abort_flag);
+        ok = ok && wait_bar(bars.sready(c & 1), (c >> 1) & 1, abort_flag);
         __syncwarp();
         tc_fence_after();
         tmem_ld<kRS>(s_base + NR * (c & 1), x);
@@ -790,15 +823,14 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       pre = false;
       if (c + 1 < nchunks) {
         const int cn = c + 1;
-        const bool rdy = mbar_test_wait(bars.ak(cn & 3), (cn >> 2) & 1) && mbar_test_wait(bars.qk(cn & 1), (cn >> 1) & 1);
+        const bool rdy = mbar_test_wait(bars.sready(cn & 1), (cn >> 1) & 1);
         if (__all_sync(kFull, rdy)) {
           tc_fence_after();
           tmem_ld<kRS>(s_base + NR * (cn & 1), x);
           pre = true;
         }
       }
-      // P'[c % 3] was read by P.V(c - 3)
-      if (c >= 3 && !wait_bar(bars.pv(c % 3), ((c - 3) / 3) & 1, abort_flag)) aborted = true;
+      // P'[c % 3] was read by P.V(c - 3), done since sready(c) is
       uint8_t* pbuf = sm + C::kP + (c % 3) * C::kPBytes;
 #pragma unroll
       for (int q = 0; q < kRS / 8; ++q)
@@ -844,16 +876,21 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       tc_fence_after();
     }
     aborted = aborted || (*abort_flag != 0u);
+    // the scratch partials of the single-launch verify are laid out
+    // [B][Hk][S][R][128] / [B][Hk][S][R] so that a CTA's rows are contiguous
+    const long fused_base = (((long)b * a.Hk + kvh) * a.S + split) * a.R;
     if (rr < kRS && qt == 0) {
       const float inv = lrow > 0.f ? 1.0f / lrow : 0.f;
       rcs[rr] = make_float2(inv * 16777216.0f, zrow * inv);  // O^T holds codes as fp16 subnormals (code * 2^-24)
       const int row = row0 + rr;
-      const float lse = aborted ? CUDART_NAN_F : (lrow > 0.f ? (-nms[rr] + log2f(lrow)) * kLn2 : -CUDART_INF_F);
-      if constexpr (FUSED) {
-        nms[128 + rr] = lse;
-      } else if (row < a.R) {
-        const long orow = (((long)(row / a.group) * a.B + b) * a.Hq + kvh * a.group + row % a.group) * a.S + split;
-        a.part_lse[orow] = lse;
+      if (row < a.R) {
+        const float lse = aborted ? CUDART_NAN_F : (lrow > 0.f ? (-nms[rr] + log2f(lrow)) * kLn2 : -CUDART_INF_F);
+        if constexpr (FUSED) {
+          a.part_lse[fused_base + row] = lse;
+        } else {
+          const long orow = ((long)(row / a.group) * a.B + b) * a.Hq + kvh * a.group + row % a.group;
+          a.part_lse[orow * a.S + split] = lse;
+        }
       }
     }
     named_bar(bar_id, 128);  // row constants ready, scr free
@@ -873,10 +910,10 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         scr[k * 128 + i] = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rc.x, rc.y);
       }
     }
-    named_bar(bar_id, 128);
-    // warp sw stores rows sw, sw + 4, ... (512 contiguous bytes each); row
-    // r = n * group + jq is walked without divisions
     if constexpr (!FUSED) {
+      named_bar(bar_id, 128);
+      // warp sw stores rows sw, sw + 4, ... (512 contiguous bytes each); row
+      // r = n * group + jq is walked without divisions
       int n = (row0 + sw) / a.group, jq = (row0 + sw) % a.group;
       float4 v[kRS / 4];
       long off[kRS / 4];
@@ -895,110 +932,82 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         if (row0 + sw + 4 * m < a.R) reinterpret_cast<float4*>(a.part_o + off[m])[lane] = v[m];
     }
     if constexpr (FUSED) {
-      // ---- stage 2: merge inside the cluster (distributed shared memory),
-      // then, with two clusters, across them through a ticket
-      cluster_sync();  // every CTA of the cluster has staged its rows
-      const int c = a.csize, nclu = a.S / a.csize;
-      const int q = (int)cluster_rank(), g = split / c;
-      const int rpc = (a.R + c - 1) / c, r_lo = q * rpc, r_hi = min(a.R, r_lo + rpc);
+      // ---- stage 2 in the same launch (a cooperative grid: every CTA is
+      // resident).  The warpgroup's rows leave scr as one bulk copy; once all
+      // S splits of this (sequence, kv-head) have written theirs, split s
+      // merges rows [s rpc, (s + 1) rpc).
+      fence_async_smem();  // scr, written by this thread, is read by the bulk copy
+      named_bar(bar_id, 128);
+      if (i == 0 && row0 < a.R) {
+        bulk_s2g(a.part_o + (fused_base + row0) * kD, smem_u32(scr), (uint32_t)(min(kRS, a.R - row0) * 512));
+        bulk_commit();
+        bulk_wait_all();
+        asm volatile("fence.proxy.async.global;\n" ::: "memory");
+        __threadfence();
+      }
+      uint32_t* arrived = a.tickets + ((long)b * a.Hk + kvh) * 4;
+      uint32_t* merged = arrived + 1;
+      volatile uint32_t* go = reinterpret_cast<volatile uint32_t*>(sm + C::kMisc + 8);
+      named_bar(15, 128 * C::kSW);  // this CTA's partial rows are written
+      if (i == 0 && j == 0) {
+        __threadfence();  // ... and visible before the arrival counts
+        atomicAdd(arrived, 1u);
+        *go = spin_until_at_least(arrived, (uint32_t)a.S) ? 1u : 0u;
+        __threadfence();
+      }
+      named_bar(15, 128 * C::kSW);
+      const bool failed = *go == 0u;
+      const int rpc = (a.R + a.S - 1) / a.S, r_lo = split * rpc, r_hi = min(a.R, r_lo + rpc);
       const int w8 = warp - 8;
-      constexpr int kMW = 4 * C::kSW;  // merging warps (a warp per row)
+      constexpr int kMW = 4 * C::kSW;  // merging warps, a warp per row, lane l: coordinates 4l .. 4l+3
+      const long pair_base = ((long)b * a.Hk + kvh) * a.S * a.R;  // split 0, row 0 of this (sequence, kv-head)
       for (int r = r_lo + w8; r < r_hi; r += kMW) {
-        const int jw = r / kRS, kr = r % kRS;
-        const uint32_t lse_at = sbase + C::kRed + jw * C::kRedWG + (128 + kr) * 4;
-        const uint32_t row_at = sbase + C::kScr + jw * C::kScrWG + kr * 512 + 16 * lane;
-        const float l = lane < c ? ld_cluster_f32(map_rank(lse_at, (uint32_t)lane)) : -CUDART_INF_F;
-        float4 v[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) v[t] = t < c ? ld_cluster_v4(map_rank(row_at, (uint32_t)t)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        float M = l;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-        const float wl = (M == -CUDART_INF_F || l == -CUDART_INF_F) ? 0.f : expf(l - M);
-        float den = wl;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
+        const long orow = ((long)(r / a.group) * a.B + b) * a.Hq + kvh * a.group + r % a.group;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float den = 0.f, wl = 0.f;
+        for (int t0 = 0; t0 < a.S; t0 += 8) {  // eight partial rows in flight
+          float4 v[8];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float w = __shfl_sync(kFull, wl, t);
-          if (t < c && w != 0.f) {  // an empty split contributes nothing
-            acc.x = fmaf(w, v[t].x, acc.x);
-            acc.y = fmaf(w, v[t].y, acc.y);
-            acc.z = fmaf(w, v[t].z, acc.z);
-            acc.w = fmaf(w, v[t].w, acc.w);
+          for (int u = 0; u < 8; ++u)
+            v[u] = t0 + u < a.S
+                       ? __ldcg(reinterpret_cast<const float4*>(a.part_o + (pair_base + (long)(t0 + u) * a.R + r) * kD) + lane)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (t0 == 0) {
+            // weights exp(lse_s - max lse) of all splits (lane s holds split s),
+            // loaded while the first rows are in flight
+            const float l = lane < a.S ? __ldcg(a.part_lse + pair_base + (long)lane * a.R + r) : -CUDART_INF_F;
+            float M = l;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+            wl = (M == -CUDART_INF_F || l == -CUDART_INF_F) ? 0.f : expf(l - M);
+            den = wl;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float w = __shfl_sync(kFull, wl, (t0 + u) & 31);
+            if (t0 + u < a.S && w != 0.f) {  // an empty split contributes nothing
+              acc.x = fmaf(w, v[u].x, acc.x);
+              acc.y = fmaf(w, v[u].y, acc.y);
+              acc.z = fmaf(w, v[u].z, acc.z);
+              acc.w = fmaf(w, v[u].w, acc.w);
+            }
           }
         }
-        const float inv = den > 0.f ? 1.f / den : 0.f;
+        const float inv = failed ? CUDART_NAN_F : (den > 0.f ? 1.f / den : 0.f);
         acc.x *= inv;
         acc.y *= inv;
         acc.z *= inv;
         acc.w *= inv;
-        const long orow = ((long)(r / a.group) * a.B + b) * a.Hq + kvh * a.group + r % a.group;
-        if (nclu == 1) {
-          reinterpret_cast<float4*>(a.out + orow * kD)[lane] = acc;
-        } else {
-          // this cluster's merged row as the partial of split g c
-          reinterpret_cast<float4*>(a.part_o + (orow * a.S + g * c) * kD)[lane] = acc;
-          if (lane == 0) a.part_lse[orow * a.S + g * c] = den > 0.f ? M + logf(den) : (den == 0.f ? -CUDART_INF_F : den);
-        }
+        reinterpret_cast<float4*>(a.out + orow * kD)[lane] = acc;
       }
-      if (nclu > 1) {
-        volatile uint32_t* last = reinterpret_cast<volatile uint32_t*>(sm + C::kMisc + 8);
-        uint32_t* ticket = a.tickets + ((long)b * a.Hk + kvh) * 4 + q;
-        named_bar(15, 128 * C::kSW);  // this CTA's merged rows are out
-        if (i == 0 && j == 0) {
-          __threadfence();
-          const uint32_t t = atomicAdd(ticket, 1u);
-          *last = t == (uint32_t)nclu - 1 ? 1u : 0u;
-          if (t == (uint32_t)nclu - 1) *ticket = 0u;  // ready for the next call
-        }
-        named_bar(15, 128 * C::kSW);
-        if (*last) {
-          __threadfence();  // the other cluster's merged rows are visible
-          for (int r = r_lo + w8; r < r_hi; r += kMW) {
-            const long orow = ((long)(r / a.group) * a.B + b) * a.Hq + kvh * a.group + r % a.group;
-            const float l = lane < nclu ? __ldcg(a.part_lse + orow * a.S + lane * c) : -CUDART_INF_F;
-            float4 v[2];
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-              v[t] = t < nclu ? __ldcg(reinterpret_cast<const float4*>(a.part_o + (orow * a.S + t * c) * kD) + lane)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-            float M = l;
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-            const float wl = (M == -CUDART_INF_F || l == -CUDART_INF_F) ? 0.f : expf(l - M);
-            float den = wl;
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const float w = __shfl_sync(kFull, wl, t);
-              if (t < nclu && w != 0.f) {
-                acc.x = fmaf(w, v[t].x, acc.x);
-                acc.y = fmaf(w, v[t].y, acc.y);
-                acc.z = fmaf(w, v[t].z, acc.z);
-                acc.w = fmaf(w, v[t].w, acc.w);
-              }
-            }
-            const float inv = den > 0.f ? 1.f / den : 0.f;
-            acc.x *= inv;
-            acc.y *= inv;
-            acc.z *= inv;
-            acc.w *= inv;
-            reinterpret_cast<float4*>(a.out + orow * kD)[lane] = acc;
-          }
-        }
+      named_bar(15, 128 * C::kSW);
+      if (i == 0 && j == 0 && atomicAdd(merged, 1u) == (uint32_t)a.S - 1u) {
+        // every split is past its wait: leave the counters zero for the next call
+        atomicExch(arrived, 0u);
+        atomicExch(merged, 0u);
       }
-      cluster_sync();  // peers may still be reading this CTA's rows
-    }
-  }
-
-  if constexpr (FUSED) {
-    if (warp < 8) {  // the softmax warps pass both inside their merge
-      cluster_sync();
-      cluster_sync();
     }
   }
 
@@ -1073,43 +1082,33 @@ cudaError_t launch_tc(const VerifyArgs& a, cudaStream_t st) {
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[0].val.programmaticStreamSerializationAllowed = 1;
-  attrs[1].id = cudaLaunchAttributeClusterDimension;
-  attrs[1].val.clusterDim.x = FUSED ? (unsigned)a.csize : 1u;
-  attrs[1].val.clusterDim.y = 1;
-  attrs[1].val.clusterDim.z = 1;
+  // the single-launch verify waits across CTAs: a cooperative launch
+  // guarantees that every CTA of the grid is resident
+  attrs[1].id = cudaLaunchAttributeCooperative;
+  attrs[1].val.cooperative = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = FUSED ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, a, tmap);
 }
 
-// how many clusters of c CTAs of the fused kernel can be resident at once
+// how many CTAs of the single-launch verify kernel can be resident at once
 template <int PRESET, int NR>
-int fused_capacity(int c) {
+int fused_capacity() {
   using C = Cfg<PRESET, NR>;
-  static std::atomic<int> known[16][5];  // per device and cluster size: 0 = not queried, else capacity + 1
+  static std::atomic<int> known[16];  // per device: 0 = not queried, else capacity + 1
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  int v = known[dev & 15][c].load(std::memory_order_acquire);
+  int v = known[dev & 15].load(std::memory_order_acquire);
   if (v == 0) {
     auto kern = verify_stage1_tc_kernel<PRESET, NR, true>;
-    int n = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) == cudaSuccess) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(c, 1, 1);
-      cfg.blockDim = dim3(C::kThreads);
-      cfg.dynamicSmemBytes = C::kSmem;
-      cudaLaunchAttribute attr;
-      attr.id = cudaLaunchAttributeClusterDimension;
-      attr.val.clusterDim.x = (unsigned)c;
-      attr.val.clusterDim.y = 1;
-      attr.val.clusterDim.z = 1;
-      cfg.attrs = &attr;
-      cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
-    }
+    int per_sm = 0, sms = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, C::kSmem) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      per_sm = sms = 0;
     cudaGetLastError();  // a refused query leaves no sticky error
-    v = n + 1;
-    known[dev & 15][c].store(v, std::memory_order_release);
+    v = per_sm * sms + 1;
+    known[dev & 15].store(v, std::memory_order_release);
   }
   return v - 1;
 }
@@ -1129,18 +1128,14 @@ cudaError_t launch_verify_stage1_tc(int preset, const VerifyArgs& a, cudaStream_
   return launch_tc<1, 64, false>(a, st);
 }
 
-bool verify_fused_supported(int preset, VerifyArgs& a) {
-  if (a.R > 64) return false;
-  const int c = a.S <= 4 ? a.S : (a.S == 6 || a.S == 8) ? a.S / 2 : 0;
-  if (c < 1) return false;
-  // every cluster resident at once: a wave of clusters would serialise the merge
-  const long clusters = (long)(a.S / c) * a.Hk * a.B;
+bool verify_fused_supported(int preset, const VerifyArgs& a) {
+  if (a.R > 64 || a.S > 32) return false;
+  // every CTA resident at once (the merge waits for all splits)
+  const long ctas = (long)a.S * a.Hk * a.B;
   int cap = 0;
-  if (preset == 0) cap = a.R <= 16 ? fused_capacity<0, 16>(c) : a.R <= 32 ? fused_capacity<0, 32>(c) : fused_capacity<0, 64>(c);
-  else cap = a.R <= 16 ? fused_capacity<1, 16>(c) : a.R <= 32 ? fused_capacity<1, 32>(c) : fused_capacity<1, 64>(c);
-  if (clusters > cap) return false;
-  a.csize = c;
-  return true;
+  if (preset == 0) cap = a.R <= 16 ? fused_capacity<0, 16>() : a.R <= 32 ? fused_capacity<0, 32>() : fused_capacity<0, 64>();
+  else cap = a.R <= 16 ? fused_capacity<1, 16>() : a.R <= 32 ? fused_capacity<1, 32>() : fused_capacity<1, 64>();
+  return ctas <= cap;
 }
 
 cudaError_t launch_verify_fused(int preset, const VerifyArgs& a, cudaStream_t st) {
