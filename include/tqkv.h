@@ -182,6 +182,26 @@ tq_status tq_verify(const tq_cache_desc* cache, const void* q, const int32_t* bl
                     int32_t Hq, int32_t num_kv_splits, int32_t causal, float* partial_o,
                     float* partial_lse, uint32_t* tickets, float* out, void* stream);
 
+/* tq_verify without caller scratch (paper has no counterpart: a convenience
+ * of this C ABI).  The partials, log-sum-exps and merge counters live in
+ * device arrays of the library itself (16 MiB of partials and log-sum-exps,
+ * 16384 counter words), so a call allocates nothing; out is the only buffer
+ * written.  Arguments, layouts, alignment and validation are those of
+ * tq_verify without partial_o, partial_lse and tickets.
+ *   Set-up: the first call on a device looks up the arrays' addresses and
+ *     clears the counters, synchronising the device; make it before any
+ *     stream capture on that device.
+ *   Sharing: every call on a device uses the same scratch.  Calls on one
+ *     device must not overlap in time (order them on one stream); calls that
+ *     run concurrently on different streams race on the scratch.
+ *   Errors: TQ_ERR_UNSUPPORTED when n_spec * B * Hq * num_kv_splits * 129
+ *     floats exceed the scratch or B * Hk * 4 exceeds the counter words (the
+ *     caller then uses tq_verify with its own buffers); TQ_ERR_CUDA when the
+ *     set-up fails; otherwise tq_verify's status. */
+tq_status tq_verify_noalloc(const tq_cache_desc* cache, const void* q, const int32_t* block_table,
+                            int32_t max_blocks, const int32_t* seq_lens, int32_t n_spec, int32_t B,
+                            int32_t Hq, int32_t num_kv_splits, int32_t causal, float* out, void* stream);
+
 /* Reads and clears the library's sticky device-side error word on the
  * current device.  Every wait of the tensor-core stage-1 kernel on a shared
  * memory barrier is bounded; when one expires the kernel gives up on its

@@ -77,6 +77,8 @@ def load(build_if_missing: bool = False):
         lib.tq_verify_stage2.argtypes = [P, P, I, I, I, I, I, P, P]
         lib.tq_verify.restype = I
         lib.tq_verify.argtypes = [D, P, P, I, P, I, I, I, I, I, P, P, P, P, P]
+        lib.tq_verify_noalloc.restype = I
+        lib.tq_verify_noalloc.argtypes = [D, P, P, I, P, I, I, I, I, I, P, P]
         lib.tq_device_status.restype = I
         lib.tq_device_status.argtypes = []
         _lib = lib
@@ -207,3 +209,22 @@ def tq_verify(cache: torch.Tensor, preset: int, q: torch.Tensor, block_table: to
                           _dev(partial_o, torch.float32, "partial_o"), _dev(partial_lse, torch.float32, "partial_lse"),
                           _dev(tickets, torch.int32, "tickets"), _dev(out, torch.float32, "out"), _stream(stream))
     _check(st, "tq_verify")
+
+
+def tq_verify_noalloc(cache: torch.Tensor, preset: int, q: torch.Tensor, block_table: torch.Tensor,
+                      seq_lens: torch.Tensor, num_kv_splits: int, causal: bool, out: torch.Tensor,
+                      stream=None) -> None:
+    """tq_verify with the library's own scratch: no partial or counter buffers.
+    The first call on a device sets the scratch up (synchronising); calls on
+    one device must not overlap."""
+    d = cache_desc(cache, preset)
+    n_spec, B, Hq, D = q.shape
+    if D != 128 or block_table.dim() != 2 or block_table.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("q [n_spec,B,Hq,128], block_table [B,max_blocks], seq_lens [B]")
+    if out.shape != (n_spec, B, Hq, 128):
+        raise ValueError("out [n_spec,B,Hq,128]")
+    st = load().tq_verify_noalloc(ctypes.byref(d), _dev(q, torch.float16, "q"),
+                                  _dev(block_table, torch.int32, "block_table"), int(block_table.shape[1]),
+                                  _dev(seq_lens, torch.int32, "seq_lens"), n_spec, B, Hq, int(num_kv_splits),
+                                  int(bool(causal)), _dev(out, torch.float32, "out"), _stream(stream))
+    _check(st, "tq_verify_noalloc")
