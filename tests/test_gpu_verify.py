@@ -252,13 +252,14 @@ FUSED = [
     ("k3v4_nc", 8, 2, 4, 2, 203, 3, False),
     ("k8v4", 1, 3, 8, 2, (17, 300), 4, True),
     ("k3v4_nc", 8, 1, 32, 4, 555, 7, True),
-    ("k8v4", 4, 2, 8, 1, 300, 8, True),     # two clusters of four
+    ("k8v4", 4, 2, 8, 1, 300, 8, True),     # eight splits: one row per split to merge
     ("k3v4_nc", 4, 2, 6, 3, 40, 1, True),
-    ("k3v4_nc", 8, 2, 16, 2, 900, 6, True),  # two clusters of three
+    ("k3v4_nc", 8, 2, 16, 2, 900, 6, True),  # rows not a multiple of the splits
     ("k8v4", 8, 1, 8, 1, 64, 8, True),      # most splits empty
     ("k8v4", 3, 2, 2, 2, 3, 5, True),       # splits mostly empty
     ("k3v4_nc", 2, 1, 16, 1, 77, 16, True),
-    ("k8v4", 2, 3, 8, 4, 700, 40, False),   # more splits than a warp's lanes
+    ("k8v4", 1, 2, 8, 1, 2000, 32, True),   # the most splits one launch merges
+    ("k8v4", 2, 3, 8, 4, 700, 40, False),   # more splits than one launch merges: two launches
     ("k8v4", 16, 1, 8, 1, 100, 3, True),    # 128 rows: mma.sync stage 1 + stage 2
 ]
 
