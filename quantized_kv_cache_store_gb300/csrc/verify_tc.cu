@@ -731,6 +731,13 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         mx0 = fmax3(mx0, d[k].x, d[k].y);
         if (k + 1 < kH) mx1 = fmax3(mx1, d[k + 1].x, d[k + 1].y);
       }
+      // p = 2^d in place, issued before the vote so that the vote's latency
+      // hides behind the exponentials; a vote for the exact path recomputes it
+      auto exps = [&]() {
+#pragma unroll
+        for (int k = 0; k < kH; ++k) d[k] = make_float2(ex2(d[k].x), ex2(d[k].y));
+      };
+      exps();
       // leave the loop together: the named barriers need all four warps
       // S^T(c) is released to the MMA issuer (for S^T(c + 2)) once no path of
       // this chunk reads it again
@@ -804,15 +811,16 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
           tc_wait_st();
         }
         scores();
+        exps();
       } else {
         release_s();
       }
-      // probabilities, row sums, zero term; P' = p * scale into the MN-major B tile
+      // row sums, zero term; P' = p * scale into the MN-major B tile
       uint32_t pk[kH];
       const float2 sv2 = make_float2(cp.y, cp.y), zv2 = make_float2(cp.z, cp.z);
 #pragma unroll
       for (int k = 0; k < kH; ++k) {
-        const float2 p = make_float2(ex2(d[k].x), ex2(d[k].y));
+        const float2 p = d[k];
         l2[k] = __fadd2_rn(l2[k], p);
         z2[k] = __ffma2_rn(p, zv2, z2[k]);
         const float2 ps = __fmul2_rn(p, sv2);
@@ -936,15 +944,16 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       // resident).  The warpgroup's rows leave scr as one bulk copy; once all
       // S splits of this (sequence, kv-head) have written theirs, split s
       // merges rows [s rpc, (s + 1) rpc).
-      fence_async_smem();  // scr, written by this thread, is read by the bulk copy
       named_bar(bar_id, 128);
-      if (i == 0 && row0 < a.R) {
-        bulk_s2g(a.part_o + (fused_base + row0) * kD, smem_u32(scr), (uint32_t)(min(kRS, a.R - row0) * 512));
-        bulk_commit();
-        bulk_wait_all();
-        asm volatile("fence.proxy.async.global;\n" ::: "memory");
-        __threadfence();
+      // warp sw stores rows sw, sw + 4, ... (512 contiguous bytes each)
+#pragma unroll
+      for (int m = 0; m < kRS / 4; ++m) {
+        const int row = row0 + sw + 4 * m;
+        if (row < a.R)
+          __stcg(reinterpret_cast<float4*>(a.part_o + (fused_base + row) * kD) + lane,
+                 reinterpret_cast<const float4*>(scr + (sw + 4 * m) * 128)[lane]);
       }
+      __threadfence();
       uint32_t* arrived = a.tickets + ((long)b * a.Hk + kvh) * 4;
       uint32_t* merged = arrived + 1;
       volatile uint32_t* go = reinterpret_cast<volatile uint32_t*>(sm + C::kMisc + 8);
