@@ -428,7 +428,7 @@ def run_ours(args):
         "config": {"workload": wl.name, "preset": wl.preset, "n_spec": wl.n_spec, "B": wl.B, "Hq": wl.Hq,
                    "Hk": wl.Hk, "D": 128, "seq_len": wl.seq_len, "cached_len": wl.seq_len - wl.n_spec,
                    "causal": wl.causal, "num_kv_splits": main["S"], "seed": main["seed"],
-                   "step": "tq_store(n_spec*B draft tokens) + tq_verify (one launch: split-KV attention + last-CTA merge)",
+                   "step": "tq_store(n_spec*B draft tokens) + tq_verify (one cooperative launch: split-KV attention + counter-synchronised merge)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: {main['n_caches']} rotating cache copies of "
                          f"{main['cache_bytes'] / 1e6:.1f} MB",
