@@ -193,6 +193,15 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// (2^lo, 2^hi) as an f16x2 pair from two fp32 exponents: one MUFU operation
+// for two values (relative error ~2^-10); -inf -> 0
+__device__ __forceinline__ uint32_t ex2_h2(float lo, float hi) {
+  uint32_t h, y;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(h));
+  return y;
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -731,11 +740,13 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         mx0 = fmax3(mx0, d[k].x, d[k].y);
         if (k + 1 < kH) mx1 = fmax3(mx1, d[k + 1].x, d[k + 1].y);
       }
-      // p = 2^d in place, issued before the vote so that the vote's latency
-      // hides behind the exponentials; a vote for the exact path recomputes it
+      // p = 2^d as fp16 pairs (the precision of the P' operand), issued
+      // before the vote so that the vote's latency hides behind the
+      // exponentials; a vote for the exact path recomputes them
+      uint32_t ph[kH];
       auto exps = [&]() {
 #pragma unroll
-        for (int k = 0; k < kH; ++k) d[k] = make_float2(ex2(d[k].x), ex2(d[k].y));
+        for (int k = 0; k < kH; ++k) ph[k] = ex2_h2(d[k].x, d[k].y);
       };
       exps();
       // leave the loop together: the named barriers need all four warps
@@ -817,14 +828,16 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       }
       // row sums, zero term; P' = p * scale into the MN-major B tile
       uint32_t pk[kH];
-      const float2 sv2 = make_float2(cp.y, cp.y), zv2 = make_float2(cp.z, cp.z);
+      const __half2 svh = __float2half2_rn(cp.y);
+      const float2 zv2 = make_float2(cp.z, cp.z);
 #pragma unroll
       for (int k = 0; k < kH; ++k) {
-        const float2 p = d[k];
+        const __half2 ph2 = *reinterpret_cast<const __half2*>(&ph[k]);
+        const float2 p = __half22float2(ph2);
         l2[k] = __fadd2_rn(l2[k], p);
         z2[k] = __ffma2_rn(p, zv2, z2[k]);
-        const float2 ps = __fmul2_rn(p, sv2);
-        pk[k] = pack_half2(ps.x, ps.y);
+        const __half2 ps = __hmul2(ph2, svh);
+        pk[k] = *reinterpret_cast<const uint32_t*>(&ps);
       }
       // start loading S^T(c + 1) if it is already there (never wait for it here:
       // this chunk's pfull would then depend on S^T(c + 1))
@@ -849,32 +862,56 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       if (lane == 0) mbar_arrive(bars.pfull(c % 3));
     }
     if (pre) tc_wait_ld();
-    // ---- epilogue: l and the zero term over all 128 tokens (transposed through
-    // scr), then the output rows O^T / l staged in scr and stored in bulk
-    float lrow = 0.f, zrow = 0.f;  // row rr, in threads with qt == 0
-#pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-      named_bar(bar_id, 128);  // scr is free
+    // ---- epilogue: l and the zero term of each row over all 128 tokens, by a
+    // reduce-scatter across the warp's lanes (each step halves the rows a lane
+    // holds) and a sum of the four warps' partials in scr; then the output
+    // rows O^T / l staged in scr and stored
+    auto reduce_rows = [&](float(&v)[kRS]) -> float {  // lane's row: lane / (32 / kRS)
+#pragma unroll
+      for (int st = 0; st < 5; ++st) {
+        const int off = 16 >> st, n = kRS >> st;
+        if (n >= 2) {
+          const bool up = (lane & off) != 0;
+#pragma unroll
+          for (int k = 0; k < n / 2; ++k) {
+            const float send = up ? v[k] : v[k + n / 2];
+            const float keep = up ? v[k + n / 2] : v[k];
+            v[k] = keep + __shfl_xor_sync(kFull, send, off);
+          }
+        } else {
+          v[0] += __shfl_xor_sync(kFull, v[0], off);
+        }
+      }
+      return v[0];
+    };
+    named_bar(bar_id, 128);  // scr is free
+    {
+      constexpr int kLanesPerRow = 32 / kRS;
+      float v[kRS];
 #pragma unroll
       for (int k = 0; k < kH; ++k) {
-        const float2 v = pass ? z2[k] : l2[k];
-        scr[tr_index(2 * k, i)] = v.x;
-        scr[tr_index(2 * k + 1, i)] = v.y;
+        v[2 * k] = l2[k].x;
+        v[2 * k + 1] = l2[k].y;
       }
-      named_bar(bar_id, 128);
-      if (rr < kRS) {
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll 1
-        for (int u = 0; u < 8; u += 2) {
-          const float4 a0 = *tr_seg(scr, rr, qt, u), a1 = *tr_seg(scr, rr, qt, u + 1);
-          s0 += (a0.x + a0.y) + (a0.z + a0.w);
-          s1 += (a1.x + a1.y) + (a1.z + a1.w);
-        }
-        float sum = s0 + s1;
-        sum += __shfl_xor_sync(kFull, sum, 1);
-        sum += __shfl_xor_sync(kFull, sum, 2);
-        if (pass) zrow = sum;
-        else lrow = sum;
+      const float lw = reduce_rows(v);
+#pragma unroll
+      for (int k = 0; k < kH; ++k) {
+        v[2 * k] = z2[k].x;
+        v[2 * k + 1] = z2[k].y;
+      }
+      const float zw = reduce_rows(v);
+      if (lane % kLanesPerRow == 0) {
+        scr[sw * 32 + lane / kLanesPerRow] = lw;
+        scr[128 + sw * 32 + lane / kLanesPerRow] = zw;
+      }
+    }
+    named_bar(bar_id, 128);
+    float lrow = 0.f, zrow = 0.f;  // row i, in threads i < kRS
+    if (i < kRS) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        lrow += scr[w * 32 + i];
+        zrow += scr[128 + w * 32 + i];
       }
     }
     if (nchunks > 0) {
@@ -887,12 +924,12 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     // the scratch partials of the single-launch verify are laid out
     // [B][Hk][S][R][128] / [B][Hk][S][R] so that a CTA's rows are contiguous
     const long fused_base = (((long)b * a.Hk + kvh) * a.S + split) * a.R;
-    if (rr < kRS && qt == 0) {
+    if (i < kRS) {
       const float inv = lrow > 0.f ? 1.0f / lrow : 0.f;
-      rcs[rr] = make_float2(inv * 16777216.0f, zrow * inv);  // O^T holds codes as fp16 subnormals (code * 2^-24)
-      const int row = row0 + rr;
+      rcs[i] = make_float2(inv * 16777216.0f, zrow * inv);  // O^T holds codes as fp16 subnormals (code * 2^-24)
+      const int row = row0 + i;
       if (row < a.R) {
-        const float lse = aborted ? CUDART_NAN_F : (lrow > 0.f ? (-nms[rr] + log2f(lrow)) * kLn2 : -CUDART_INF_F);
+        const float lse = aborted ? CUDART_NAN_F : (lrow > 0.f ? (-nms[i] + log2f(lrow)) * kLn2 : -CUDART_INF_F);
         if constexpr (FUSED) {
           a.part_lse[fused_base + row] = lse;
         } else {
