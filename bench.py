@@ -212,14 +212,14 @@ def bench_workload(name, args, rank, world, pg, dev_props):
 
     # eager warm-up of each entry point (first-call set-up happens outside capture)
     with torch.cuda.stream(stream):
-        sv.step_fused(0)
+        sv.step_one(0)
     torch.cuda.synchronize()
-    step_graph = capture(G, 0, lambda i: sv.step_fused(i))
+    step_graph = capture(G, 0, lambda i: sv.step_one(i))
     # K steps = full replays of G plus one shorter graph for the remainder
     full, rem = divmod(args.steps, G)
-    rem_graph = capture(rem, 0, lambda i: sv.step_fused(i)) if rem else None
+    rem_graph = capture(rem, 0, lambda i: sv.step_one(i)) if rem else None
     wfull, wrem = divmod(max(args.warmup, 3), G)
-    wrem_graph = capture(wrem, 0, lambda i: sv.step_fused(i)) if wrem else None
+    wrem_graph = capture(wrem, 0, lambda i: sv.step_one(i)) if wrem else None
 
     def run(nfull, tail):
         for _ in range(nfull):
@@ -255,11 +255,11 @@ def bench_workload(name, args, rank, world, pg, dev_props):
 
     # per-kernel durations: each launch bracketed by external events in a graph
     kern_us = per_kernel_durations(sv, stream, G, n_caches)
-    # the roofline kernel: the verify launch that reads the cache (the
-    # single-launch tq_verify when it applies, else stage 1)
-    fused = kern_us.get("tq_verify_fused") if kern_us else None
+    # the roofline kernel: the launch that reads the cache (the step's single
+    # launch, tq_store_verify, when it applies, else stage 1)
+    fused = kern_us.get("tq_store_verify") if kern_us else None
     stage1_us = fused if fused else (kern_us["tq_verify_stage1"] if kern_us else None)
-    roof_kernel = "tq_verify (single launch)" if fused else "tq_verify_stage1"
+    roof_kernel = "tq_store_verify (single launch)" if fused else "tq_verify_stage1"
 
     # verify-only (stage 1 + 2) throughput, same graph method
     vgraph = capture(G, 0, lambda i: sv.verify_call(i))
@@ -290,6 +290,16 @@ def bench_workload(name, args, rank, world, pg, dev_props):
                 clocks=clk, alg_bytes=alg_bytes, G=G, stream=stream)
 
 
+def single_launch(sv) -> bool:
+    """Whether tq_verify / tq_store_verify run as one cooperative launch:
+    up to 64 rows per kv-head, up to 32 splits, every CTA resident (one per SM)."""
+    import torch
+
+    wl = sv.wl
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return wl.n_spec * wl.Hq // wl.Hk <= 64 and sv.S <= 32 and sv.S * wl.Hk * wl.B <= sms
+
+
 def per_kernel_durations(sv, stream, G, n_caches):
     """Average duration of each kernel: a CUDA graph of G launches of that
     kernel alone (the cache copy rotating as in the step), timed with events
@@ -305,8 +315,9 @@ def per_kernel_durations(sv, stream, G, n_caches):
                                                             sv.part_lse, stream),
         "tq_verify_stage2": lambda c: tqkv.tq_verify_stage2(sv.part_o, sv.part_lse, sv.out, stream),
     }
-    if sv.wl.n_spec * sv.wl.Hq // sv.wl.Hk <= 64:  # tq_verify is one launch
+    if single_launch(sv):  # tq_verify and tq_store_verify are one launch each
         calls["tq_verify_fused"] = lambda c: sv.verify_call(c, stream)
+        calls["tq_store_verify"] = lambda c: sv.step_one(c, stream)
     out = {}
     for name, fn in calls.items():
         g = torch.cuda.CUDAGraph()
@@ -328,7 +339,7 @@ def per_kernel_durations(sv, stream, G, n_caches):
 
 def e2e_measure(res, args):
     """Same step through the public API with HOST buffers: pinned host -> device
-    copies of the step's inputs, the three calls, device -> host copy of the
+    copies of the step's inputs, the tq_store_verify call, device -> host copy of the
     result, every step, eager (no graph)."""
     import torch
 
@@ -338,9 +349,8 @@ def e2e_measure(res, args):
     h_q = inp.q.contiguous().pin_memory()
     h_k = inp.k[drafts].contiguous().pin_memory()
     h_v = inp.v[drafts].contiguous().pin_memory()
-    h_s = torch.from_numpy(inp.slots[drafts]).contiguous().pin_memory()
     h_out = torch.empty(sv.out.shape, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_s))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v))
     d2h = h_out.numel() * h_out.element_size()
     n = max(1, min(args.e2e_steps, args.steps))
 
@@ -348,8 +358,7 @@ def e2e_measure(res, args):
         sv.q.copy_(h_q, non_blocking=True)
         sv.k_new.copy_(h_k, non_blocking=True)
         sv.v_new.copy_(h_v, non_blocking=True)
-        sv.slots_new.copy_(h_s, non_blocking=True)
-        sv.step_fused(i % res["n_caches"], stream)
+        sv.step_one(i % res["n_caches"], stream)
         h_out.copy_(sv.out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -428,7 +437,7 @@ def run_ours(args):
         "config": {"workload": wl.name, "preset": wl.preset, "n_spec": wl.n_spec, "B": wl.B, "Hq": wl.Hq,
                    "Hk": wl.Hk, "D": 128, "seq_len": wl.seq_len, "cached_len": wl.seq_len - wl.n_spec,
                    "causal": wl.causal, "num_kv_splits": main["S"], "seed": main["seed"],
-                   "step": "tq_store(n_spec*B draft tokens) + tq_verify (one cooperative launch: split-KV attention + counter-synchronised merge)",
+                   "step": "tq_store_verify: store of the n_spec*B draft tokens + split-KV attention + counter-synchronised merge, one cooperative launch",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: {main['n_caches']} rotating cache copies of "
                          f"{main['cache_bytes'] / 1e6:.1f} MB",
@@ -438,7 +447,7 @@ def run_ours(args):
         "roofline": main["roofline"],
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (1 if single_launch(main["sv"]) else 3) * args.steps,
         "clocks": main["clocks"],
         "also": also,
     }

@@ -182,6 +182,25 @@ tq_status tq_verify(const tq_cache_desc* cache, const void* q, const int32_t* bl
                     int32_t Hq, int32_t num_kv_splits, int32_t causal, float* partial_o,
                     float* partial_lse, uint32_t* tickets, float* out, void* stream);
 
+/* One verify step: store each sequence's n_spec draft tokens into the cache
+ * (tq_store), then verify them (tq_verify).  The pages run the store and the
+ * attention as separate kernels ("spec-decode-intel-arc", section "Context":
+ * the fused store is one of the three hot kernels; section "Part 3").  Draft n
+ * of sequence b goes to position p = min(seq_lens[b], max_blocks * 16) -
+ * n_spec + n, i.e. page block_table[b][p / 16], offset p % 16 (a negative p
+ * or an out-of-range block id skips the draft), with the bytes tq_store
+ * writes.  Where tq_verify runs as one launch, the CTA whose page range holds
+ * a draft stores it before copying that page; otherwise a store launch and
+ * tq_verify are enqueued.
+ * Arguments are those of tq_verify plus
+ *   k_new, v_new  fp16 [B][n_spec][Hk][128], 16-byte aligned: the drafts'
+ *                 keys and values (the cache is written, so it must not be
+ *                 read by other work in flight). */
+tq_status tq_store_verify(const tq_cache_desc* cache, const void* k_new, const void* v_new, const void* q,
+                          const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
+                          int32_t n_spec, int32_t B, int32_t Hq, int32_t num_kv_splits, int32_t causal,
+                          float* partial_o, float* partial_lse, uint32_t* tickets, float* out, void* stream);
+
 /* tq_verify without caller scratch (paper has no counterpart: a convenience
  * of this C ABI).  The partials, log-sum-exps and merge counters live in
  * device arrays of the library itself (16 MiB of partials and log-sum-exps,

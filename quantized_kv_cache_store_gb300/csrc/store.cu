@@ -1,184 +1,11 @@
 // store.cu -- the fused store kernel of libtqkv: quantise and bit-pack new
 // K/V tokens into the paged cache ("spec-decode-intel-arc", section
-// "Context": the fused store is one of the three hot kernels; keys are
-// Walsh-Hadamard rotated and coded against a Lloyd-Max codebook, or stored as
-// FP8; values are uniform-scalar quantised with a scale and a zero).
-//
-// One warp per (token, kv-head); lane l owns coordinates 4l .. 4l+3.  All fp32
-// arithmetic uses explicitly rounded intrinsics (__fadd_rn, __fmul_rn,
-// __fdiv_rn, __fsqrt_rn) so that no step is contracted into an FMA and the
-// cache bytes are a fixed function of the inputs:
-//   |k|^2  = lane partial (x0^2 + x1^2) + (x2^2 + x3^2), then xor-butterfly
-//            rounds at lane offsets 16, 8, 4, 2, 1;
-//   H k    = unnormalised Sylvester butterflies, stride 1, 2 in-lane, then
-//            strides 4..64 across lanes (offset stride / 4), (a + b, a - b);
-//   y      = (H k) / (|k| * sqrt(128)),  code = #{boundaries strictly below y};
-//   nc     = fp16(|k| / sqrt(|c_hat|^2)) with |c_hat|^2 summed in the same order.
-#include <cuda_fp8.h>
-
-#include "tq_common.cuh"
+// "Context": the fused store is one of the three hot kernels).  One warp per
+// (token, kv-head); the arithmetic is store_ops.cuh's.
+#include "store_ops.cuh"
 
 namespace tq {
 namespace {
-
-constexpr unsigned kFull = 0xffffffffu;
-
-__device__ __forceinline__ float half_bits_to_float(uint16_t b) {
-  return __half2float(__ushort_as_half(b));
-}
-
-__device__ __forceinline__ float tree_sum(float a0, float a1, float a2, float a3) {
-  float s = __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3));
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) s = __fadd_rn(s, __shfl_xor_sync(kFull, s, off));
-  return s;
-}
-
-// fp16 -> e4m3, round to nearest even, saturating; NaN -> 0x7F.
-__device__ __forceinline__ uint32_t e4m3_of_half(uint16_t h) {
-  __half2_raw pair;
-  pair.x = h;
-  pair.y = 0;
-  uint32_t b = (uint32_t)(__nv_cvt_halfraw2_to_fp8x2(pair, __NV_SATFINITE, __NV_E4M3) & 0xFFu);
-  uint32_t mag = h & 0x7FFFu;
-  if (mag > 0x7C00u) b = 0x7Fu;                        // NaN
-  else if (mag == 0x7C00u) b = (h & 0x8000u) ? 0xFEu : 0x7Eu;  // +-inf saturates
-  return b;
-}
-
-__device__ __forceinline__ void store_key8(uint8_t* page, int off, int lane, const uint16_t h[4]) {
-  uint32_t w = e4m3_of_half(h[0]) | (e4m3_of_half(h[1]) << 8) | (e4m3_of_half(h[2]) << 16) |
-               (e4m3_of_half(h[3]) << 24);
-  *reinterpret_cast<uint32_t*>(page + K8::kKey + off * kD + 4 * lane) = w;
-}
-
-__device__ __forceinline__ void store_key3(uint8_t* page, int off, int lane, const uint16_t h[4],
-                                           const Codebook& cb) {
-  float x[4], t[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[i] = half_bits_to_float(h[i]);
-    t[i] = x[i];
-  }
-  const float ss = tree_sum(__fmul_rn(x[0], x[0]), __fmul_rn(x[1], x[1]), __fmul_rn(x[2], x[2]),
-                            __fmul_rn(x[3], x[3]));
-  const float norm = __fsqrt_rn(ss);
-  // stride 1 and 2 inside the lane
-  {
-    float a = t[0], b = t[1];
-    t[0] = __fadd_rn(a, b);
-    t[1] = __fsub_rn(a, b);
-    a = t[2];
-    b = t[3];
-    t[2] = __fadd_rn(a, b);
-    t[3] = __fsub_rn(a, b);
-    a = t[0];
-    b = t[2];
-    t[0] = __fadd_rn(a, b);
-    t[2] = __fsub_rn(a, b);
-    a = t[1];
-    b = t[3];
-    t[1] = __fadd_rn(a, b);
-    t[3] = __fsub_rn(a, b);
-  }
-  // strides 4 .. 64 across lanes: the lower index holds a, the upper holds b
-#pragma unroll
-  for (int o = 1; o <= 16; o <<= 1) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float p = __shfl_xor_sync(kFull, t[i], o);
-      t[i] = upper ? __fsub_rn(p, t[i]) : __fadd_rn(t[i], p);
-    }
-  }
-  float C[8], Bd[7];
-#pragma unroll
-  for (int m = 0; m < 8; ++m) C[m] = half_bits_to_float(cb.c[m]);
-#pragma unroll
-  for (int m = 0; m < 7; ++m) Bd[m] = __fmul_rn(__fadd_rn(C[m], C[m + 1]), 0.5f);
-  const float denom = __fmul_rn(norm, __fsqrt_rn(128.0f));
-  uint32_t code[4];
-  float c2[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float y = (norm == 0.0f) ? 0.0f : __fdiv_rn(t[i], denom);
-    uint32_t idx = 0;
-#pragma unroll
-    for (int m = 0; m < 7; ++m) idx += (y > Bd[m]) ? 1u : 0u;
-    code[i] = idx;
-    float c = C[0];
-#pragma unroll
-    for (int m = 1; m < 8; ++m) c = (idx == (uint32_t)m) ? C[m] : c;
-    c2[i] = __fmul_rn(c, c);
-  }
-  const float cn2 = tree_sum(c2[0], c2[1], c2[2], c2[3]);
-  // 12 bits per lane at stream bit 12 * lane; 48 bytes = 12 little-endian words
-  const uint32_t bits = code[0] | (code[1] << 3) | (code[2] << 6) | (code[3] << 9);
-  const int w = lane;  // output word handled by lanes 0..11
-  uint64_t word = 0;
-  const int first = (32 * w) / 12;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int src = min(first + j, 31);
-    const uint32_t val = __shfl_sync(kFull, bits, src);
-    const int shift = 12 * src - 32 * w;  // position of src's bits inside this word
-    if (first + j <= 31 && shift > -12 && shift < 32) {
-      word |= shift >= 0 ? ((uint64_t)val << shift) : ((uint64_t)val >> (-shift));
-    }
-  }
-  if (lane < 12)
-    *reinterpret_cast<uint32_t*>(page + K3::kKey + off * 48 + 4 * w) = (uint32_t)(word & 0xFFFFFFFFull);
-  if (lane == 0) {
-    const uint16_t nc = (norm == 0.0f) ? (uint16_t)0
-                                       : __half_as_ushort(__float2half_rn(__fdiv_rn(norm, __fsqrt_rn(cn2))));
-    *reinterpret_cast<uint16_t*>(page + K3::kNc + 2 * off) = nc;
-  }
-}
-
-template <class L>
-__device__ __forceinline__ void store_value4(uint8_t* page, int off, int lane, const uint16_t h[4]) {
-  float v[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = half_bits_to_float(h[i]);
-  float lo = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
-  float hi = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-#pragma unroll
-  for (int off2 = 16; off2 >= 1; off2 >>= 1) {
-    lo = fminf(lo, __shfl_xor_sync(kFull, lo, off2));
-    hi = fmaxf(hi, __shfl_xor_sync(kFull, hi, off2));
-  }
-  const __half zh = __float2half_rn(__fadd_rn(lo, 0.0f));  // -0 -> +0
-  uint16_t sh = 0;
-  if (hi != lo) {
-    const float r = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
-    sh = __half_as_ushort(__float2half_rn(r));
-    if (half_bits_to_float(sh) < r) sh = (uint16_t)(sh + 1);  // round the scale up
-  }
-  const float zf = __half2float(zh), sf = half_bits_to_float(sh);
-  uint32_t c[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float qv = 0.0f;
-    if (sh != 0) qv = rintf(__fdiv_rn(__fsub_rn(v[i], zf), sf));
-    qv = fminf(fmaxf(qv, 0.0f), 15.0f);
-    c[i] = (uint32_t)qv;
-  }
-  // codes are stored coordinate-major: byte 8d + off/2, low nibble = even off.
-  // Tokens of one page share bytes, so each nibble is replaced atomically.
-  uint32_t* vw = reinterpret_cast<uint32_t*>(page + L::kVal);
-  const int nib = 4 * (off & 7);
-  const uint32_t keep = ~(0xFu << nib);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t* w = vw + 2 * (4 * lane + i) + (off >> 3);
-    atomicAnd(w, keep);
-    atomicOr(w, c[i] << nib);
-  }
-  if (lane == 0) {
-    *reinterpret_cast<uint16_t*>(page + L::kScale + 2 * off) = sh;
-    *reinterpret_cast<uint16_t*>(page + L::kZero + 2 * off) = __half_as_ushort(zh);
-  }
-}
 
 template <int PRESET>
 __global__ void __launch_bounds__(128) store_kernel(StoreArgs a) {
@@ -190,7 +17,16 @@ __global__ void __launch_bounds__(128) store_kernel(StoreArgs a) {
   if (unit >= (long)a.T * a.Hk) return;
   const long t = unit / a.Hk;
   const int h = (int)(unit % a.Hk);
-  const int32_t slot = a.slots[t];
+  int32_t slot;
+  if (a.slots) {
+    slot = a.slots[t];
+  } else {  // draft n of sequence b at position L_b - n_spec + n
+    const int b = (int)(t / a.n_spec), n = (int)(t % a.n_spec);
+    const int L = max(0, min(a.seq_lens[b], a.max_blocks * kBlock));
+    const int pos = L - a.n_spec + n;
+    const int id = pos >= 0 ? a.block_table[(long)b * a.max_blocks + pos / kBlock] : -1;
+    slot = (id >= 0 && id < a.num_blocks) ? id * kBlock + pos % kBlock : -1;
+  }
   if (slot < 0 || slot >= a.num_blocks * kBlock) return;  // skipped token (warp-uniform)
   const int blk = slot / kBlock, off = slot % kBlock;
   uint8_t* page = a.cache + ((long)blk * a.Hk + h) * L::kPage;
@@ -201,11 +37,7 @@ __global__ void __launch_bounds__(128) store_kernel(StoreArgs a) {
                           (uint16_t)(kr.y >> 16)};
   const uint16_t vh[4] = {(uint16_t)(vr.x & 0xFFFF), (uint16_t)(vr.x >> 16), (uint16_t)(vr.y & 0xFFFF),
                           (uint16_t)(vr.y >> 16)};
-  if (PRESET == 0)
-    store_key8(page, off, lane, kh);
-  else
-    store_key3(page, off, lane, kh, a.cb);
-  store_value4<L>(page, off, lane, vh);
+  store_ops::store_token<PRESET>(page, off, lane, kh, vh, a.cb);
 }
 
 }  // namespace

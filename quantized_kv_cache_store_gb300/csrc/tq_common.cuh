@@ -48,8 +48,14 @@ struct StoreArgs {
   int Hk;
   const __half* k;
   const __half* v;
-  const int32_t* slots;
+  const int32_t* slots;  // [T]; null: the drafts of a verify step, slots from the block table
   int T;
+  // with slots == null: token t = b * n_spec + n goes to position
+  // min(seq_lens[b], max_blocks * 16) - n_spec + n of sequence b
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* seq_lens;
+  int n_spec;
   Codebook cb;
 };
 
@@ -66,6 +72,11 @@ struct VerifyArgs {
   float* part_lse;
   float* out;         // merged output (single-launch verify only)
   uint32_t* tickets;  // [B][Hk][4], zero between calls (single-launch verify only)
+  // drafts to store first (single-launch store + verify only, else null):
+  // fp16 [B][n_spec][Hk][128], draft n of sequence b at position L_b - n_spec + n
+  const __half* dk;
+  const __half* dv;
+  uint8_t* cache_w;   // the cache, writable (same as cache)
   Codebook cb;
 };
 

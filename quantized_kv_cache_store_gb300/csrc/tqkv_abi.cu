@@ -109,6 +109,9 @@ tq_status verify_args(const tq_cache_desc* cache, const void* q, const int32_t* 
   a.part_lse = partial_lse;
   a.out = nullptr;
   a.tickets = nullptr;
+  a.dk = nullptr;
+  a.dv = nullptr;
+  a.cache_w = nullptr;
   a.cb = codebook();
   return TQ_OK;
 }
@@ -161,6 +164,10 @@ tq_status tq_store(const tq_cache_desc* cache, const void* k, const void* v, con
   a.v = static_cast<const __half*>(v);
   a.slots = slot_mapping;
   a.T = T;
+  a.block_table = nullptr;
+  a.max_blocks = 0;
+  a.seq_lens = nullptr;
+  a.n_spec = 0;
   a.cb = codebook();
   return from_cuda(tq::launch_store(cache->preset, a, static_cast<cudaStream_t>(stream)));
 }
@@ -197,6 +204,49 @@ tq_status tq_verify(const tq_cache_desc* cache, const void* q, const int32_t* bl
 }
 
 
+
+tq_status tq_store_verify(const tq_cache_desc* cache, const void* k_new, const void* v_new, const void* q,
+                          const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens, int32_t n_spec,
+                          int32_t B, int32_t Hq, int32_t num_kv_splits, int32_t causal, float* partial_o,
+                          float* partial_lse, uint32_t* tickets, float* out, void* stream) {
+  tq::VerifyArgs a;
+  tq_status s = verify_args(cache, q, block_table, max_blocks, seq_lens, n_spec, B, Hq, num_kv_splits, causal,
+                            partial_o, partial_lse, &a);
+  if (s != TQ_OK) return s;
+  if (!out || !tickets || !k_new || !v_new) return TQ_ERR_INVALID_ARG;
+  if ((long)cache->num_blocks * 16 > INT32_MAX) return TQ_ERR_UNSUPPORTED;
+  if (!aligned(out, 16) || !aligned(tickets, 4) || !aligned(k_new, 16) || !aligned(v_new, 16))
+    return TQ_ERR_MISALIGNED;
+  if (B == 0) return TQ_OK;
+  a.out = out;
+  a.tickets = tickets;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (tq::verify_fused_supported(cache->preset, a)) {
+    a.dk = static_cast<const __half*>(k_new);
+    a.dv = static_cast<const __half*>(v_new);
+    a.cache_w = static_cast<uint8_t*>(cache->cache);
+    return from_cuda(tq::launch_verify_fused(cache->preset, a, st));
+  }
+  // otherwise the drafts go through the store kernel (slots from the block
+  // table), then tq_verify
+  tq::StoreArgs sa;
+  sa.cache = static_cast<uint8_t*>(cache->cache);
+  sa.num_blocks = cache->num_blocks;
+  sa.Hk = cache->num_kv_heads;
+  sa.k = static_cast<const __half*>(k_new);
+  sa.v = static_cast<const __half*>(v_new);
+  sa.slots = nullptr;
+  sa.T = n_spec * B;
+  sa.block_table = block_table;
+  sa.max_blocks = max_blocks;
+  sa.seq_lens = seq_lens;
+  sa.n_spec = n_spec;
+  sa.cb = codebook();
+  s = from_cuda(tq::launch_store(cache->preset, sa, st));
+  if (s != TQ_OK) return s;
+  return tq_verify(cache, q, block_table, max_blocks, seq_lens, n_spec, B, Hq, num_kv_splits, causal, partial_o,
+                   partial_lse, tickets, out, stream);
+}
 
 tq_status tq_verify_stage2(const float* partial_o, const float* partial_lse, int32_t n_spec, int32_t B,
                            int32_t Hq, int32_t head_dim, int32_t num_kv_splits, float* out, void* stream) {

@@ -50,6 +50,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include "store_ops.cuh"
 #include "tc_ptx.cuh"
 #include "tq_common.cuh"
 
@@ -115,9 +116,9 @@ struct Cfg {
   static constexpr int kPair = kScr + kSW * kScrWG;  // u32 [64][32] (k3v4_nc)
   static constexpr int kPValid = kPair + (PRESET == 1 ? 64 * 32 * 4 : 0);  // u8 [kStages][8]
   static constexpr int kBar = align_up(kPValid + kStages * 8, 8);
-  // full[kStages] empty[kStages] ak[4] sready[2] pfull[3] pv[3] sfree[2] av[3]
+  // full[kStages] empty[kStages] ak[4] sready[2] pfull[3] pv[3] sfree[2] av[3] dstored
   static constexpr int kProducers = 3;  // warps 0, 2, 3 copy pages 0-2, 3-5, 6-7 of a chunk
-  static constexpr int kNumBars = 2 * kStages + 17;
+  static constexpr int kNumBars = 2 * kStages + 18;
   static constexpr int kMisc = kBar + 8 * kNumBars;  // u32 tmem base, u32 abort
   static constexpr int kSmem = kMisc + 16 + 1024;    // + alignment slack
   // tensor memory columns
@@ -148,6 +149,7 @@ struct Bars {
   __device__ uint32_t pv(int i) const { return base + 8 * (2 * stages + 9 + i); }     // O^T += V^T P'^T done (c % 3)
   __device__ uint32_t sfree(int b) const { return base + 8 * (2 * stages + 12 + b); } // S^T(c) read by the softmax (c % 2)
   __device__ uint32_t av(int i) const { return base + 8 * (2 * stages + 14 + i); }    // A_V written (c % 3)
+  __device__ uint32_t dstored() const { return base + 8 * (2 * stages + 17); }        // drafts written (once)
 };
 
 // Bounded wait for a global counter written by other CTAs of the same
@@ -296,6 +298,13 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
   const int page_lo = t_lo / kBlock;
   const int npages = t_hi > t_lo ? (t_hi - t_lo + kBlock - 1) / kBlock : 0;
   const int nchunks = (npages + C::kPages - 1) / C::kPages;
+  // single-launch store + verify: this split first stores the drafts at
+  // positions [d_lo, t_hi) (the drafts sit at [L_b - n_spec, L_b), and the
+  // splits are page-aligned, so no other CTA reads their pages); chunks from
+  // c_draft on are copied only after that
+  const int d_lo = max(max(L_b - a.n_spec, t_lo), 0);
+  const bool stores = FUSED && a.dk != nullptr && d_lo < t_hi;
+  const int c_draft = stores ? (d_lo - t_lo) / (C::kPages * kBlock) : nchunks;
   const int32_t* bt = a.block_table + (long)b * a.max_blocks;
 
   // Producers = warps 0, 2, 3 (C::kProducers): producer w copies pages
@@ -360,6 +369,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       mbar_init(bars.sready(i), 5);
       mbar_init(bars.sfree(i), 4 * C::kSW);
     }
+    mbar_init(bars.dstored(), 4 * C::kSW);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -372,7 +382,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
   // the first kStages chunks need no free slot: issue them before the prologue
   // only chunk 0 goes out before the prologue: with every CTA streaming its
   // whole ring at once the first chunk would land last
-  const int prefill = min(nchunks, 1);
+  const int prefill = c_draft == 0 ? 0 : min(nchunks, 1);
   if (producer)
     for (int c = 0; c < prefill; ++c) produce(c);
 
@@ -454,11 +464,12 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       // ================= producers: their pages of each chunk into the ring
       int c = prefill;
       for (; c < nchunks; ++c) {
-        if ((c & 3) == 0) {
+        if ((c & 3) == 0 && c > 0) {  // group 0's ids are loaded before the set-up
           ids = ids_next;
           ids_next = fetch_ids(c + 4);  // lands while this group is copied
         }
         if (!wait_bar(bars.empty(c % C::kStages), ((c / C::kStages) - 1) & 1, abort_flag)) break;
+        if (c == c_draft && !wait_bar(bars.dstored(), 0, abort_flag)) break;
         produce(c);
       }
       // drain: copies still in flight must land before the CTA can exit
@@ -659,6 +670,31 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     }
   } else {
     regs_inc<C::kRegSm>();
+    if constexpr (FUSED) {
+      if (stores) {
+        // the drafts of this split, one warp per draft, while the first scores
+        // are still on their way; then released to the producers
+        for (int n = warp - 8; n < a.n_spec; n += 4 * C::kSW) {
+          const int pos = L_b - a.n_spec + n;
+          if (pos < d_lo || pos >= t_hi) continue;
+          const int id = a.block_table[(long)b * a.max_blocks + pos / kBlock];
+          if (id < 0 || id >= a.num_blocks) continue;
+          uint8_t* page = a.cache_w + ((long)id * a.Hk + kvh) * L::kPage;
+          const long base = (((long)b * a.n_spec + n) * a.Hk + kvh) * kD + 4 * lane;
+          const uint2 kr = *reinterpret_cast<const uint2*>(a.dk + base);
+          const uint2 vr = *reinterpret_cast<const uint2*>(a.dv + base);
+          const uint16_t kh[4] = {(uint16_t)(kr.x & 0xFFFF), (uint16_t)(kr.x >> 16), (uint16_t)(kr.y & 0xFFFF),
+                                  (uint16_t)(kr.y >> 16)};
+          const uint16_t vh[4] = {(uint16_t)(vr.x & 0xFFFF), (uint16_t)(vr.x >> 16), (uint16_t)(vr.y & 0xFFFF),
+                                  (uint16_t)(vr.y >> 16)};
+          store_ops::store_token<PRESET>(page, pos % kBlock, lane, kh, vh, a.cb);
+        }
+        // the pages' new bytes, written through the generic proxy, are read next by bulk copies
+        asm volatile("fence.proxy.async.global;\n" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.dstored());
+      }
+    }
     // ================= softmax warpgroup j: thread i = TMEM lane i = token i,
     // query rows [row0, row0 + kRS)
     constexpr int kH = kRS / 2;

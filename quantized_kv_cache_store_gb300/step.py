@@ -76,3 +76,10 @@ class SpecVerify:
         """Store the drafts, then one tq_verify call."""
         self.store(i, stream)
         return self.verify_call(i, stream)
+
+    def step_one(self, i: int = 0, stream=None) -> torch.Tensor:
+        """The whole step as one tq_store_verify call (one launch where possible)."""
+        tqkv.tq_store_verify(self.caches[i], self.preset, self.k_new, self.v_new, self.q, self.block_table,
+                             self.seq_lens, self.S, self.wl.causal, self.part_o, self.part_lse, self.tickets,
+                             self.out, stream)
+        return self.out

@@ -77,6 +77,8 @@ def load(build_if_missing: bool = False):
         lib.tq_verify_stage2.argtypes = [P, P, I, I, I, I, I, P, P]
         lib.tq_verify.restype = I
         lib.tq_verify.argtypes = [D, P, P, I, P, I, I, I, I, I, P, P, P, P, P]
+        lib.tq_store_verify.restype = I
+        lib.tq_store_verify.argtypes = [D, P, P, P, P, I, P, I, I, I, I, I, P, P, P, P, P]
         lib.tq_verify_noalloc.restype = I
         lib.tq_verify_noalloc.argtypes = [D, P, P, I, P, I, I, I, I, I, P, P]
         lib.tq_device_status.restype = I
@@ -209,6 +211,34 @@ def tq_verify(cache: torch.Tensor, preset: int, q: torch.Tensor, block_table: to
                           _dev(partial_o, torch.float32, "partial_o"), _dev(partial_lse, torch.float32, "partial_lse"),
                           _dev(tickets, torch.int32, "tickets"), _dev(out, torch.float32, "out"), _stream(stream))
     _check(st, "tq_verify")
+
+
+def tq_store_verify(cache: torch.Tensor, preset: int, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+                    block_table: torch.Tensor, seq_lens: torch.Tensor, num_kv_splits: int, causal: bool,
+                    partial_o: torch.Tensor, partial_lse: torch.Tensor, tickets: torch.Tensor, out: torch.Tensor,
+                    stream=None) -> None:
+    """Store the drafts (k_new, v_new: fp16 [B * n_spec, Hk, 128], sequence-major)
+    at the last n_spec positions of each sequence, then verify (one launch
+    where tq_verify takes one)."""
+    d = cache_desc(cache, preset)
+    n_spec, B, Hq, D = q.shape
+    if k_new.shape != (B * n_spec, d.num_kv_heads, 128) or v_new.shape != k_new.shape:
+        raise ValueError("k_new and v_new must be [B * n_spec, Hk, 128]")
+    if D != 128 or block_table.dim() != 2 or block_table.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("q [n_spec,B,Hq,128], block_table [B,max_blocks], seq_lens [B]")
+    S = int(num_kv_splits)
+    if partial_o.shape != (n_spec, B, Hq, S, 128) or partial_lse.shape != (n_spec, B, Hq, S):
+        raise ValueError("partial_o [n_spec,B,Hq,S,128] and partial_lse [n_spec,B,Hq,S]")
+    if out.shape != (n_spec, B, Hq, 128) or tickets.shape != (B, d.num_kv_heads, 4):
+        raise ValueError("out [n_spec,B,Hq,128], tickets [B,Hk,4]")
+    st = load().tq_store_verify(ctypes.byref(d), _dev(k_new, torch.float16, "k_new"),
+                                _dev(v_new, torch.float16, "v_new"), _dev(q, torch.float16, "q"),
+                                _dev(block_table, torch.int32, "block_table"), int(block_table.shape[1]),
+                                _dev(seq_lens, torch.int32, "seq_lens"), n_spec, B, Hq, S, int(bool(causal)),
+                                _dev(partial_o, torch.float32, "partial_o"),
+                                _dev(partial_lse, torch.float32, "partial_lse"), _dev(tickets, torch.int32, "tickets"),
+                                _dev(out, torch.float32, "out"), _stream(stream))
+    _check(st, "tq_store_verify")
 
 
 def tq_verify_noalloc(cache: torch.Tensor, preset: int, q: torch.Tensor, block_table: torch.Tensor,

@@ -127,3 +127,17 @@ def test_single_call_validation(lib):
     assert v(q=0) == tqkv.TQ_ERR_INVALID_ARG
     assert v(S=0) == tqkv.TQ_ERR_INVALID_ARG
     assert v(B=0) == tqkv.TQ_OK  # nothing to enqueue
+
+
+def test_store_verify_validation(lib):
+    d = _desc(ptr=FAKE)
+    v = lambda k=FAKE, vv=FAKE, q=FAKE, t=FAKE, out=FAKE, B=1: lib.tq_store_verify(
+        ctypes.byref(d), k, vv, q, FAKE, 4, FAKE, 8, B, 32, 2, 1, FAKE, FAKE, t, out, None)
+    assert v(k=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert v(vv=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert v(out=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert v(k=FAKE + 8) == tqkv.TQ_ERR_MISALIGNED
+    assert v(vv=FAKE + 2) == tqkv.TQ_ERR_MISALIGNED
+    assert v(t=FAKE + 2) == tqkv.TQ_ERR_MISALIGNED
+    assert v(q=0) == tqkv.TQ_ERR_INVALID_ARG
+    assert v(B=0) == tqkv.TQ_OK  # nothing to enqueue
