@@ -376,6 +376,59 @@ def e2e_measure(res, args):
             "d2h_bytes_per_step": d2h, "steps": n, "mode": "eager C-ABI calls, pinned host buffers"}
 
 
+def isolated_latency(res, reps=20):
+    """One step at a time after an L2 flush (a 256 MB write): median of reps
+    event-timed single calls, each on a cold L2 and an idle GPU."""
+    import torch
+
+    sv, stream = res["sv"], res["stream"]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=sv.device)
+    times = []
+    for i in range(reps):
+        with torch.cuda.stream(stream):
+            flush.fill_(i & 255)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            sv.step_one(i % res["n_caches"], stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3)
+    return round(statistics.median(times), 3)
+
+
+def store_throughput(res, reps=5):
+    """tq_store of every cached prefix token (the untimed cache fill of a
+    step, HBM-write bound): device-resident fp16 K/V, event-timed, best of reps.
+    Bytes = fp16 K and V read + cache slots written."""
+    import torch
+
+    from quantized_kv_cache_store_gb300 import tqkv
+
+    sv, inp, stream = res["sv"], res["inp"], res["stream"]
+    rows = inp.prefix_rows()[: 1 << 18]
+    k = inp.k[rows].to(sv.device)
+    v = inp.v[rows].to(sv.device)
+    sl = torch.from_numpy(inp.slots[rows]).to(sv.device)
+    cache = sv.caches[-1]
+    best = None
+    for _ in range(reps):
+        with torch.cuda.stream(stream):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            tqkv.tq_store(cache, sv.preset, k, v, sl, stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) * 1e3
+        best = t if best is None else min(best, t)
+    th = len(rows) * sv.wl.Hk
+    nbytes = th * (2 * 128 * 2 + tqkv.tq_page_bytes(sv.preset) // 16)
+    # the cache copy written here is restored, so later steps see the same bytes
+    cache.copy_(sv.caches[0])
+    torch.cuda.synchronize()
+    return {"token_heads": th, "us": round(best, 3), "GB/s": round(nbytes / (best * 1e-6) / 1e9, 1),
+            "bytes": nbytes}
+
+
 def cpu_baseline(res, budget_s=12.0):
     """The oracle as it stands (C, OpenMP over (sequence, kv-head)) on the
     host cores: store of the step's draft tokens + fp64 verify of every row,
@@ -417,6 +470,8 @@ def run_ours(args):
     props = torch.cuda.get_device_properties(torch.cuda.current_device())
     main = bench_workload(args.workload, args, rank, world, pg, props)
     e2e = e2e_measure(main, args)
+    iso_us = isolated_latency(main)
+    store_tp = store_throughput(main)
     also = {}
     for name in [x for x in args.also.split(",") if x and x != args.workload]:
         r = bench_workload(name, args, rank, world, pg, props)
@@ -447,6 +502,8 @@ def run_ours(args):
         "roofline": main["roofline"],
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "isolated_us": iso_us,
+        "store_prefill": store_tp,
         "gpu_launches": (1 if single_launch(main["sv"]) else 3) * args.steps,
         "clocks": main["clocks"],
         "also": also,

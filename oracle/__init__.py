@@ -26,6 +26,7 @@ _lib = None
 
 PRESET_K8V4 = 0
 PRESET_K3V4_NC = 1
+PRESET_K3V4 = 2  # k3v4_nc's coding with the plain norm as key factor
 HEAD_DIM = 128
 BLOCK = 16
 

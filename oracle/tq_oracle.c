@@ -48,7 +48,10 @@
 #define D 128
 #define BLK 16
 
-enum { PRESET_K8V4 = 0, PRESET_K3V4_NC = 1 };
+enum { PRESET_K8V4 = 0, PRESET_K3V4_NC = 1, PRESET_K3V4 = 2 };
+/* k3v4_nc and k3v4 share the key coding and the page; k3v4 stores the plain
+ * norm |k| as the key factor instead of the corrected |k| / |c_hat| */
+static int is_k3(int preset) { return preset == PRESET_K3V4_NC || preset == PRESET_K3V4; }
 
 /* Planar page layout for one (block, kv-head), 16 tokens (value codes stored
  * coordinate-major: 128 coordinates x 8 bytes of 16 nibbles).  Byte budgets:
@@ -70,7 +73,7 @@ enum { PRESET_K8V4 = 0, PRESET_K3V4_NC = 1 };
 
 long oracle_page_bytes(int preset) {
   if (preset == PRESET_K8V4) return K8_PAGE;
-  if (preset == PRESET_K3V4_NC) return K3_PAGE;
+  if (is_k3(preset)) return K3_PAGE;
   return -1;
 }
 
@@ -285,10 +288,12 @@ void oracle_unpack3(const uint8_t in[48], uint8_t idx[D]) {
 static void put_h(uint8_t* p, uint16_t h) { p[0] = (uint8_t)(h & 255); p[1] = (uint8_t)(h >> 8); }
 static uint16_t get_h(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
 
-/* k3v4_nc key encoder for one token-head: norm, rotation, nearest centroid,
- * bit packing, norm correction.  Writes 48 code bytes and the fp16 nc. */
-void oracle_encode_key3(const uint16_t k[D], const uint16_t cb[8], uint8_t codes[48],
-                        uint16_t* nc_out) {
+/* k3 key encoder for one token-head: norm, rotation, nearest centroid, bit
+ * packing, and the fp16 key factor: |k| / |c_hat| (norm correction, preset
+ * k3v4_nc) when corrected, else |k| (preset k3v4).  Writes 48 code bytes and
+ * the factor. */
+void oracle_encode_key3_factor(const uint16_t k[D], const uint16_t cb[8], uint8_t codes[48],
+                               uint16_t* nc_out, int corrected) {
   float x[D], sq[D], t[D];
   for (int j = 0; j < D; ++j) {
     x[j] = oracle_h2f(k[j]);
@@ -308,8 +313,15 @@ void oracle_encode_key3(const uint16_t k[D], const uint16_t cb[8], uint8_t codes
     c2[j] = c * c;
   }
   float cn2 = oracle_tree_sum(c2);
-  *nc_out = (norm == 0.0f) ? 0 : oracle_f2h_rn(norm / sqrtf(cn2));
+  if (!corrected) *nc_out = oracle_f2h_rn(norm);
+  else *nc_out = (norm == 0.0f) ? 0 : oracle_f2h_rn(norm / sqrtf(cn2));
   oracle_pack3(idx, codes);
+}
+
+/* k3v4_nc key encoder (norm correction). */
+void oracle_encode_key3(const uint16_t k[D], const uint16_t cb[8], uint8_t codes[48],
+                        uint16_t* nc_out) {
+  oracle_encode_key3_factor(k, cb, codes, nc_out, 1);
 }
 
 /* k8v4 key encoder: per-coordinate e4m3, coordinate order kept. */
@@ -371,7 +383,7 @@ int oracle_store(int preset, uint8_t* cache, int num_blocks, int Hk, const uint1
   long pb = oracle_page_bytes(preset);
   if (pb < 0) return -1;
   uint16_t cb[8];
-  if (preset == PRESET_K3V4_NC) oracle_codebook16(cb);
+  if (is_k3(preset)) oracle_codebook16(cb);
   /* heads own disjoint pages, so they can be encoded in parallel; tokens of
    * one head share value-code bytes and are encoded in order */
 #pragma omp parallel for schedule(static)
@@ -393,7 +405,7 @@ int oracle_store(int preset, uint8_t* cache, int num_blocks, int Hk, const uint1
         put_h(page + K8_Z_OFF + 2 * off, z);
       } else {
         uint16_t nc;
-        oracle_encode_key3(kk, cb, page + K3_K_OFF + off * 48, &nc);
+        oracle_encode_key3_factor(kk, cb, page + K3_K_OFF + off * 48, &nc, preset == PRESET_K3V4_NC);
         put_h(page + K3_NC_OFF + 2 * off, nc);
         put_value_codes(page + K3_V_OFF, off, code);
         put_h(page + K3_S_OFF + 2 * off, s);
@@ -564,7 +576,7 @@ static void make_source(kv_source* src, int preset, const uint8_t* cache, int nu
   src->g = g;
   src->bt = bt_row;
   src->max_blocks = max_blocks;
-  if (preset == PRESET_K3V4_NC) oracle_codebook16(src->cb);
+  if (is_k3(preset)) oracle_codebook16(src->cb);
 }
 
 /* Spec-verify attention for a list of output rows.  Each row is (n, b, h):

@@ -46,8 +46,9 @@ cudaError_t launch_store(int preset, const StoreArgs& a, cudaStream_t st) {
   const long units = (long)a.T * a.Hk;
   if (units == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((units + 3) / 4);
-  return preset == 0 ? launch_pdl(store_kernel<0>, dim3(grid), dim3(128), 0, st, a)
-                      : launch_pdl(store_kernel<1>, dim3(grid), dim3(128), 0, st, a);
+  if (preset == 0) return launch_pdl(store_kernel<0>, dim3(grid), dim3(128), 0, st, a);
+  if (preset == 1) return launch_pdl(store_kernel<1>, dim3(grid), dim3(128), 0, st, a);
+  return launch_pdl(store_kernel<2>, dim3(grid), dim3(128), 0, st, a);
 }
 
 }  // namespace tq

@@ -52,8 +52,10 @@ __device__ __forceinline__ void store_key8(uint8_t* page, int off, int lane, con
   *reinterpret_cast<uint32_t*>(page + K8::kKey + off * kD + 4 * lane) = w;
 }
 
+// k3 keys; the fp16 key factor is |k| / |c_hat| (norm correction, k3v4_nc)
+// when corrected, else |k| (k3v4)
 __device__ __forceinline__ void store_key3(uint8_t* page, int off, int lane, const uint16_t h[4],
-                                           const Codebook& cb) {
+                                           const Codebook& cb, bool corrected = true) {
   float x[4], t[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -129,8 +131,9 @@ __device__ __forceinline__ void store_key3(uint8_t* page, int off, int lane, con
   if (lane < 12)
     *reinterpret_cast<uint32_t*>(page + K3::kKey + off * 48 + 4 * w) = (uint32_t)(word & 0xFFFFFFFFull);
   if (lane == 0) {
-    const uint16_t nc = (norm == 0.0f) ? (uint16_t)0
-                                       : __half_as_ushort(__float2half_rn(__fdiv_rn(norm, __fsqrt_rn(cn2))));
+    const uint16_t nc = !corrected ? __half_as_ushort(__float2half_rn(norm))
+                        : (norm == 0.0f) ? (uint16_t)0
+                                         : __half_as_ushort(__float2half_rn(__fdiv_rn(norm, __fsqrt_rn(cn2))));
     *reinterpret_cast<uint16_t*>(page + K3::kNc + 2 * off) = nc;
   }
 }
@@ -184,12 +187,12 @@ __device__ __forceinline__ void store_value4(uint8_t* page, int off, int lane, c
 // in kh / vh) into offset off of its page
 template <int PRESET>
 __device__ __forceinline__ void store_token(uint8_t* page, int off, int lane, const uint16_t kh[4],
-                                            const uint16_t vh[4], const Codebook& cb) {
+                                            const uint16_t vh[4], const Codebook& cb, bool plain_norm = PRESET == 2) {
   using L = Layout<PRESET>;
   if (PRESET == 0)
     store_key8(page, off, lane, kh);
   else
-    store_key3(page, off, lane, kh, cb);
+    store_key3(page, off, lane, kh, cb, !plain_norm);
   store_value4<L>(page, off, lane, vh);
 }
 

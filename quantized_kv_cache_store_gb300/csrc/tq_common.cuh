@@ -36,6 +36,9 @@ template <>
 struct Layout<0> : K8 {};
 template <>
 struct Layout<1> : K3 {};
+// k3v4: k3v4_nc's page, the plain norm |k| as key factor
+template <>
+struct Layout<2> : K3 {};
 
 // Eight fp16 centroids, ascending, passed to kernels by value.
 struct Codebook {
@@ -77,6 +80,7 @@ struct VerifyArgs {
   const __half* dk;
   const __half* dv;
   uint8_t* cache_w;   // the cache, writable (same as cache)
+  int plain_norm;     // preset k3v4: drafts stored with the plain norm as key factor
   Codebook cb;
 };
 

@@ -58,14 +58,15 @@ const tq::Codebook& codebook() {
 
 size_t page_bytes(int32_t preset) {
   if (preset == TQ_PRESET_K8V4) return tq::K8::kPage;
-  if (preset == TQ_PRESET_K3V4_NC) return tq::K3::kPage;
+  if (preset == TQ_PRESET_K3V4_NC || preset == TQ_PRESET_K3V4) return tq::K3::kPage;
   return 0;
 }
 
 tq_status check_desc(const tq_cache_desc* d) {
   if (!d || !d->cache) return TQ_ERR_INVALID_ARG;
   if (d->num_kv_heads < 1 || d->num_blocks < 0 || d->reserved != 0) return TQ_ERR_INVALID_ARG;
-  if (d->preset != TQ_PRESET_K8V4 && d->preset != TQ_PRESET_K3V4_NC) return TQ_ERR_UNSUPPORTED;
+  if (d->preset != TQ_PRESET_K8V4 && d->preset != TQ_PRESET_K3V4_NC && d->preset != TQ_PRESET_K3V4)
+    return TQ_ERR_UNSUPPORTED;
   if (d->head_dim != 128 || d->block_size != 16) return TQ_ERR_UNSUPPORTED;
   if (d->num_kv_heads > 65535) return TQ_ERR_UNSUPPORTED;
   if (!aligned(d->cache, 16)) return TQ_ERR_MISALIGNED;
@@ -112,6 +113,7 @@ tq_status verify_args(const tq_cache_desc* cache, const void* q, const int32_t* 
   a.dk = nullptr;
   a.dv = nullptr;
   a.cache_w = nullptr;
+  a.plain_norm = cache->preset == TQ_PRESET_K3V4 ? 1 : 0;
   a.cb = codebook();
   return TQ_OK;
 }
@@ -129,7 +131,8 @@ size_t tq_partials_bytes(int32_t n_spec, int32_t B, int32_t Hq, int32_t num_kv_s
 
 tq_status tq_codebook(int32_t preset, float* centroids_out) {
   if (!centroids_out) return TQ_ERR_INVALID_ARG;
-  if (preset != TQ_PRESET_K3V4_NC) return preset == TQ_PRESET_K8V4 ? TQ_ERR_UNSUPPORTED : TQ_ERR_INVALID_ARG;
+  if (preset != TQ_PRESET_K3V4_NC && preset != TQ_PRESET_K3V4)
+    return preset == TQ_PRESET_K8V4 ? TQ_ERR_UNSUPPORTED : TQ_ERR_INVALID_ARG;
   const tq::Codebook& cb = codebook();
   for (int i = 0; i < 8; ++i) centroids_out[i] = __half2float(__ushort_as_half(cb.c[i]));
   return TQ_OK;

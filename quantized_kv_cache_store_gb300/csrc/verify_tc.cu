@@ -687,7 +687,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
                                   (uint16_t)(kr.y >> 16)};
           const uint16_t vh[4] = {(uint16_t)(vr.x & 0xFFFF), (uint16_t)(vr.x >> 16), (uint16_t)(vr.y & 0xFFFF),
                                   (uint16_t)(vr.y >> 16)};
-          store_ops::store_token<PRESET>(page, pos % kBlock, lane, kh, vh, a.cb);
+          store_ops::store_token<PRESET>(page, pos % kBlock, lane, kh, vh, a.cb, a.plain_norm != 0);
         }
         // the pages' new bytes, written through the generic proxy, are read next by bulk copies
         asm volatile("fence.proxy.async.global;\n" ::: "memory");

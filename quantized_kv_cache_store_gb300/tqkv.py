@@ -24,7 +24,8 @@ TQ_ERR_CUDA = 4
 TQ_ERR_TIMEOUT = 5
 TQ_PRESET_K8V4 = 0
 TQ_PRESET_K3V4_NC = 1
-PRESETS = {"k8v4": TQ_PRESET_K8V4, "k3v4_nc": TQ_PRESET_K3V4_NC}
+TQ_PRESET_K3V4 = 2
+PRESETS = {"k8v4": TQ_PRESET_K8V4, "k3v4_nc": TQ_PRESET_K3V4_NC, "k3v4": TQ_PRESET_K3V4}
 
 _lock = threading.Lock()
 _lib = None

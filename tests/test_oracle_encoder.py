@@ -117,6 +117,29 @@ def test_norm_correction_preserves_norm(oracle_lib):
             assert abs(np.linalg.norm(kh) / nk - 1.0) <= 2.0 ** -10
 
 
+def test_plain_norm_preset_differs_only_in_the_factor(oracle_lib):
+    """Preset k3v4 codes keys exactly like k3v4_nc and stores fp16(|k|) as the
+    key factor: its pages equal k3v4_nc's except in the factor field, the
+    factor is |k| to fp16 rounding, and the decoded key keeps the centroid
+    vector's own norm, |k_hat| = factor * |c_hat| (H / sqrt(D) is orthonormal)."""
+    O = oracle_lib
+    rng = np.random.default_rng(14)
+    cb = O.codebook16().view(np.float16).astype(np.float64)
+    for scale in (0.01, 1.0, 30.0):
+        for _ in range(10):
+            k = (rng.standard_normal(D) * scale).astype(np.float16)
+            v = rng.standard_normal(D).astype(np.float16)
+            pnc = _one_token_page(O, 1, k, v)
+            ppl = _one_token_page(O, 2, k, v)
+            diff = np.nonzero(pnc != ppl)[0]
+            assert set(diff) <= {768, 769}  # the fp16 factor of token 0
+            fac = float(ppl[768:770].view(np.float16)[0])
+            nk = np.linalg.norm(k.astype(np.float64))
+            assert abs(fac / nk - 1.0) <= 2.0 ** -11
+            chat = np.linalg.norm(cb[O.unpack3(ppl[0:48])])
+            assert abs(np.linalg.norm(O.decode_key(2, ppl, 0)) - fac * chat) <= 1e-12 * fac * chat
+
+
 def test_key3_distortion_matches_lloyd_max(oracle_lib):
     """Mean relative squared error of norm-corrected 3-bit keys: with
     distortion d = 0.03454 of the unit-Gaussian Lloyd-Max quantiser, the
