@@ -138,8 +138,10 @@ __device__ __forceinline__ void store_key3(uint8_t* page, int off, int lane, con
   }
 }
 
+// the value quantiser of one (token, kv-head): writes its fp16 scale and
+// zero (lane 0) and returns the 4-bit codes of the lane's 4 coordinates
 template <class L>
-__device__ __forceinline__ void store_value4(uint8_t* page, int off, int lane, const uint16_t h[4]) {
+__device__ __forceinline__ void value4_codes(uint8_t* page, int off, int lane, const uint16_t h[4], uint32_t c[4]) {
   float v[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) v[i] = half_bits_to_float(h[i]);
@@ -158,7 +160,6 @@ __device__ __forceinline__ void store_value4(uint8_t* page, int off, int lane, c
     if (half_bits_to_float(sh) < r) sh = (uint16_t)(sh + 1);  // round the scale up
   }
   const float zf = __half2float(zh), sf = half_bits_to_float(sh);
-  uint32_t c[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     float qv = 0.0f;
@@ -166,20 +167,31 @@ __device__ __forceinline__ void store_value4(uint8_t* page, int off, int lane, c
     qv = fminf(fmaxf(qv, 0.0f), 15.0f);
     c[i] = (uint32_t)qv;
   }
-  // codes are stored coordinate-major: byte 8d + off/2, low nibble = even off.
-  // Tokens of one page share bytes, so each nibble is replaced atomically.
-  uint32_t* vw = reinterpret_cast<uint32_t*>(page + L::kVal);
-  const int nib = 4 * (off & 7);
-  const uint32_t keep = ~(0xFu << nib);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t* w = vw + 2 * (4 * lane + i) + (off >> 3);
-    atomicAnd(w, keep);
-    atomicOr(w, c[i] << nib);
-  }
   if (lane == 0) {
     *reinterpret_cast<uint16_t*>(page + L::kScale + 2 * off) = sh;
     *reinterpret_cast<uint16_t*>(page + L::kZero + 2 * off) = __half_as_ushort(zh);
+  }
+}
+
+// Value codes are stored coordinate-major: the 32-bit word vword(lane, i, off)
+// of the value block holds coordinate 4 lane + i of tokens 8 (off / 8) ..
+// 8 (off / 8) + 7, token off in bits vnib(off) .. vnib(off) + 3.
+__device__ __forceinline__ int vword(int lane, int i, int off) { return 2 * (4 * lane + i) + (off >> 3); }
+__device__ __forceinline__ int vnib(int off) { return 4 * (off & 7); }
+
+template <class L>
+__device__ __forceinline__ void store_value4(uint8_t* page, int off, int lane, const uint16_t h[4]) {
+  uint32_t c[4];
+  value4_codes<L>(page, off, lane, h, c);
+  // tokens of one page share words, so each nibble is replaced atomically
+  uint32_t* vw = reinterpret_cast<uint32_t*>(page + L::kVal);
+  const int nib = vnib(off);
+  const uint32_t keep = ~(0xFu << nib);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t* w = vw + vword(lane, i, off);
+    atomicAnd(w, keep);
+    atomicOr(w, c[i] << nib);
   }
 }
 
