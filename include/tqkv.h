@@ -56,8 +56,11 @@ typedef enum {
   TQ_PRESET_K8V4 = 0,     /* keys e4m3 (RNE, saturating), values 4-bit         */
   TQ_PRESET_K3V4_NC = 1,  /* keys: WHT + 3-bit Lloyd-Max codes + fp16 norm
                              correction |k| / |c_hat|; values 4-bit            */
-  TQ_PRESET_K3V4 = 2      /* as k3v4_nc (same page), but the fp16 key factor is
+  TQ_PRESET_K3V4 = 2,     /* as k3v4_nc (same page), but the fp16 key factor is
                              the plain norm |k| (no correction)                */
+  TQ_PRESET_K3V4_NC_RS = 3 /* as k3v4_nc, keys rotated by H diag(s) / sqrt(128):
+                             s_j = -1 where the top bit of output j of
+                             SplitMix64 seeded 0x54515F5349474E53 is set      */
 } tq_preset;
 
 /* Description of a caller-owned paged cache in device memory.

@@ -27,6 +27,7 @@ _lib = None
 PRESET_K8V4 = 0
 PRESET_K3V4_NC = 1
 PRESET_K3V4 = 2  # k3v4_nc's coding with the plain norm as key factor
+PRESET_K3V4_NC_RS = 3  # k3v4_nc with a randomised-sign Hadamard rotation
 HEAD_DIM = 128
 BLOCK = 16
 
@@ -75,6 +76,10 @@ def _load():
             lib.oracle_pack3.argtypes = [P, P]
             lib.oracle_unpack3.argtypes = [P, P]
             lib.oracle_encode_key3.argtypes = [P, P, P, P]
+            lib.oracle_splitmix64.restype = ctypes.c_uint64
+            lib.oracle_splitmix64.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+            lib.oracle_rs_sign.restype = I
+            lib.oracle_rs_sign.argtypes = [I]
             lib.oracle_encode_key8.argtypes = [P, P]
             lib.oracle_encode_value4.argtypes = [P, P, P, P]
             lib.oracle_store.restype = I
@@ -181,6 +186,16 @@ def unpack3(b) -> np.ndarray:
     out = np.zeros(HEAD_DIM, np.uint8)
     _load().oracle_unpack3(_ptr(b), _ptr(out))
     return out
+
+
+def splitmix64(seed: int, j: int) -> int:
+    """Output j (0-based) of SplitMix64 seeded with seed."""
+    return int(_load().oracle_splitmix64(seed, j))
+
+
+def rs_signs() -> np.ndarray:
+    """The sign vector s of preset k3v4_nc_rs (keys rotated by H diag(s))."""
+    return np.array([_load().oracle_rs_sign(j) for j in range(128)], np.int32)
 
 
 def encode_key3(k) -> tuple[np.ndarray, int]:

@@ -48,10 +48,29 @@
 #define D 128
 #define BLK 16
 
-enum { PRESET_K8V4 = 0, PRESET_K3V4_NC = 1, PRESET_K3V4 = 2 };
-/* k3v4_nc and k3v4 share the key coding and the page; k3v4 stores the plain
- * norm |k| as the key factor instead of the corrected |k| / |c_hat| */
-static int is_k3(int preset) { return preset == PRESET_K3V4_NC || preset == PRESET_K3V4; }
+enum { PRESET_K8V4 = 0, PRESET_K3V4_NC = 1, PRESET_K3V4 = 2, PRESET_K3V4_NC_RS = 3 };
+/* k3v4_nc, k3v4 and k3v4_nc_rs share the key coding and the page; k3v4
+ * stores the plain norm |k| as the key factor instead of the corrected
+ * |k| / |c_hat|; k3v4_nc_rs rotates by H diag(s) instead of H, s a fixed
+ * random sign vector */
+static int is_k3(int preset) {
+  return preset == PRESET_K3V4_NC || preset == PRESET_K3V4 || preset == PRESET_K3V4_NC_RS;
+}
+
+/* SplitMix64 (Steele, Lea and Flood; the output function as published by
+ * Vigna): output j of the generator seeded with seed is
+ * mix(seed + (j + 1) * 0x9E3779B97F4A7C15). */
+uint64_t oracle_splitmix64(uint64_t seed, uint64_t j) {
+  uint64_t z = seed + (j + 1) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+/* The sign vector of preset k3v4_nc_rs: s_j = -1 where the top bit of output
+ * j of SplitMix64 seeded with 0x54515F5349474E53 ("TQ_SIGNS") is set. */
+#define RS_SEED 0x54515F5349474E53ull
+int oracle_rs_sign(int j) { return (oracle_splitmix64(RS_SEED, (uint64_t)j) >> 63) ? -1 : 1; }
 
 /* Planar page layout for one (block, kv-head), 16 tokens (value codes stored
  * coordinate-major: 128 coordinates x 8 bytes of 16 nibbles).  Byte budgets:
@@ -293,12 +312,12 @@ static uint16_t get_h(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8));
  * k3v4_nc) when corrected, else |k| (preset k3v4).  Writes 48 code bytes and
  * the factor. */
 void oracle_encode_key3_factor(const uint16_t k[D], const uint16_t cb[8], uint8_t codes[48],
-                               uint16_t* nc_out, int corrected) {
+                               uint16_t* nc_out, int corrected, int signed_rotation) {
   float x[D], sq[D], t[D];
   for (int j = 0; j < D; ++j) {
     x[j] = oracle_h2f(k[j]);
     sq[j] = x[j] * x[j];
-    t[j] = x[j];
+    t[j] = signed_rotation && oracle_rs_sign(j) < 0 ? -x[j] : x[j];
   }
   float ss = oracle_tree_sum(sq);
   float norm = sqrtf(ss);
@@ -321,7 +340,7 @@ void oracle_encode_key3_factor(const uint16_t k[D], const uint16_t cb[8], uint8_
 /* k3v4_nc key encoder (norm correction). */
 void oracle_encode_key3(const uint16_t k[D], const uint16_t cb[8], uint8_t codes[48],
                         uint16_t* nc_out) {
-  oracle_encode_key3_factor(k, cb, codes, nc_out, 1);
+  oracle_encode_key3_factor(k, cb, codes, nc_out, 1, 0);
 }
 
 /* k8v4 key encoder: per-coordinate e4m3, coordinate order kept. */
@@ -405,7 +424,8 @@ int oracle_store(int preset, uint8_t* cache, int num_blocks, int Hk, const uint1
         put_h(page + K8_Z_OFF + 2 * off, z);
       } else {
         uint16_t nc;
-        oracle_encode_key3_factor(kk, cb, page + K3_K_OFF + off * 48, &nc, preset == PRESET_K3V4_NC);
+        oracle_encode_key3_factor(kk, cb, page + K3_K_OFF + off * 48, &nc, preset != PRESET_K3V4,
+                                  preset == PRESET_K3V4_NC_RS);
         put_h(page + K3_NC_OFF + 2 * off, nc);
         put_value_codes(page + K3_V_OFF, off, code);
         put_h(page + K3_S_OFF + 2 * off, s);
@@ -433,6 +453,9 @@ void oracle_decode_key(int preset, const uint8_t* page, int off, const uint16_t 
   oracle_wht_f64(out);
   double nc = (double)oracle_h2f(get_h(page + K3_NC_OFF + 2 * off));
   for (int j = 0; j < D; ++j) out[j] = nc * out[j] / sqrt((double)D);
+  /* k3v4_nc_rs: the encoder rotated by H diag(s), whose inverse is diag(s) H / D */
+  if (preset == PRESET_K3V4_NC_RS)
+    for (int j = 0; j < D; ++j) out[j] *= (double)oracle_rs_sign(j);
 }
 
 /* Decoded value: v_hat = code * scale + zero, fp64. */

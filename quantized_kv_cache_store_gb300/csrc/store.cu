@@ -61,13 +61,13 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
       if (PRESET == 0)
         store_ops::store_key8(page, off, lane, kh);
       else
-        store_ops::store_key3(page, off, lane, kh, a.cb, PRESET == 1);
+        store_ops::store_key3(page, off, lane, kh, a.cb, a.plain_norm == 0, store_ops::lane_signs(a.signs, lane));
       uint32_t c[4];
       store_ops::value4_codes<L>(page, off, lane, vh, c);
 #pragma unroll
       for (int i = 0; i < 4; ++i) atomicOr(&words[4 * lane + i], c[i] << store_ops::vnib(off));
     } else {
-      store_ops::store_token<PRESET>(page, off, lane, kh, vh, a.cb);
+      store_ops::store_token<PRESET>(page, off, lane, kh, vh, a.cb, a.plain_norm != 0, store_ops::lane_signs(a.signs, lane));
     }
   }
   if (run8) {  // uniform across the CTA
@@ -86,9 +86,9 @@ cudaError_t launch_store(int preset, const StoreArgs& a, cudaStream_t st) {
   const long units = ((long)a.T + 7) / 8 * a.Hk;  // (group of 8 tokens, kv-head): one CTA each
   if (units == 0) return cudaSuccess;
   const unsigned grid = (unsigned)units;
-  if (preset == 0) return launch_pdl(store_kernel<0>, dim3(grid), dim3(256), 0, st, a);
-  if (preset == 1) return launch_pdl(store_kernel<1>, dim3(grid), dim3(256), 0, st, a);
-  return launch_pdl(store_kernel<2>, dim3(grid), dim3(256), 0, st, a);
+  // the k3 presets differ only in runtime flags (a.plain_norm, a.signs)
+  return preset == 0 ? launch_pdl(store_kernel<0>, dim3(grid), dim3(256), 0, st, a)
+                      : launch_pdl(store_kernel<1>, dim3(grid), dim3(256), 0, st, a);
 }
 
 }  // namespace tq

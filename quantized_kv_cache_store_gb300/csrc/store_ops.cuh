@@ -53,14 +53,15 @@ __device__ __forceinline__ void store_key8(uint8_t* page, int off, int lane, con
 }
 
 // k3 keys; the fp16 key factor is |k| / |c_hat| (norm correction, k3v4_nc)
-// when corrected, else |k| (k3v4)
+// when corrected, else |k| (k3v4); bit i of signs flips the lane's coordinate
+// i before the rotation (randomised-sign Hadamard, k3v4_nc_rs)
 __device__ __forceinline__ void store_key3(uint8_t* page, int off, int lane, const uint16_t h[4],
-                                           const Codebook& cb, bool corrected = true) {
+                                           const Codebook& cb, bool corrected = true, uint32_t signs = 0u) {
   float x[4], t[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     x[i] = half_bits_to_float(h[i]);
-    t[i] = x[i];
+    t[i] = ((signs >> i) & 1u) ? -x[i] : x[i];
   }
   const float ss = tree_sum(__fmul_rn(x[0], x[0]), __fmul_rn(x[1], x[1]), __fmul_rn(x[2], x[2]),
                             __fmul_rn(x[3], x[3]));
@@ -197,14 +198,20 @@ __device__ __forceinline__ void store_value4(uint8_t* page, int off, int lane, c
 
 // one (token, kv-head): 128 fp16 key and value coordinates (4 per lane, bits
 // in kh / vh) into offset off of its page
+// the 4 sign bits of lane's coordinates 4 lane .. 4 lane + 3
+__device__ __forceinline__ uint32_t lane_signs(const uint32_t signs[4], int lane) {
+  return (signs[lane >> 3] >> (4 * (lane & 7))) & 0xFu;
+}
+
 template <int PRESET>
 __device__ __forceinline__ void store_token(uint8_t* page, int off, int lane, const uint16_t kh[4],
-                                            const uint16_t vh[4], const Codebook& cb, bool plain_norm = PRESET == 2) {
+                                            const uint16_t vh[4], const Codebook& cb, bool plain_norm = PRESET == 2,
+                                            uint32_t signs = 0u) {
   using L = Layout<PRESET>;
   if (PRESET == 0)
     store_key8(page, off, lane, kh);
   else
-    store_key3(page, off, lane, kh, cb, !plain_norm);
+    store_key3(page, off, lane, kh, cb, !plain_norm, signs);
   store_value4<L>(page, off, lane, vh);
 }
 

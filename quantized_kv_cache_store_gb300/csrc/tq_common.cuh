@@ -59,6 +59,8 @@ struct StoreArgs {
   int max_blocks;
   const int32_t* seq_lens;
   int n_spec;
+  int plain_norm;      // preset k3v4: the plain norm as key factor
+  uint32_t signs[4];   // preset k3v4_nc_rs: bit j set where coordinate j's sign is flipped
   Codebook cb;
 };
 
@@ -81,6 +83,7 @@ struct VerifyArgs {
   const __half* dv;
   uint8_t* cache_w;   // the cache, writable (same as cache)
   int plain_norm;     // preset k3v4: drafts stored with the plain norm as key factor
+  uint32_t signs[4];  // preset k3v4_nc_rs: bit j set where coordinate j's sign is flipped
   Codebook cb;
 };
 

@@ -56,17 +56,39 @@ const tq::Codebook& codebook() {
   return cb;
 }
 
+// The sign vector of preset k3v4_nc_rs, as a mask (bit j set: s_j = -1):
+// s_j = -1 where the top bit of output j of SplitMix64 (the output function
+// published by Vigna) seeded with 0x54515F5349474E53 ("TQ_SIGNS") is set.
+struct SignMask {
+  uint32_t w[4];
+};
+SignMask rs_signs(int32_t preset) {
+  SignMask m = {{0u, 0u, 0u, 0u}};
+  if (preset != TQ_PRESET_K3V4_NC_RS) return m;
+  for (int j = 0; j < 128; ++j) {
+    uint64_t z = 0x54515F5349474E53ull + (uint64_t)(j + 1) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    if (z >> 63) m.w[j >> 5] |= 1u << (j & 31);
+  }
+  return m;
+}
+
+bool is_k3(int32_t preset) {
+  return preset == TQ_PRESET_K3V4_NC || preset == TQ_PRESET_K3V4 || preset == TQ_PRESET_K3V4_NC_RS;
+}
+
 size_t page_bytes(int32_t preset) {
   if (preset == TQ_PRESET_K8V4) return tq::K8::kPage;
-  if (preset == TQ_PRESET_K3V4_NC || preset == TQ_PRESET_K3V4) return tq::K3::kPage;
+  if (is_k3(preset)) return tq::K3::kPage;
   return 0;
 }
 
 tq_status check_desc(const tq_cache_desc* d) {
   if (!d || !d->cache) return TQ_ERR_INVALID_ARG;
   if (d->num_kv_heads < 1 || d->num_blocks < 0 || d->reserved != 0) return TQ_ERR_INVALID_ARG;
-  if (d->preset != TQ_PRESET_K8V4 && d->preset != TQ_PRESET_K3V4_NC && d->preset != TQ_PRESET_K3V4)
-    return TQ_ERR_UNSUPPORTED;
+  if (d->preset != TQ_PRESET_K8V4 && !is_k3(d->preset)) return TQ_ERR_UNSUPPORTED;
   if (d->head_dim != 128 || d->block_size != 16) return TQ_ERR_UNSUPPORTED;
   if (d->num_kv_heads > 65535) return TQ_ERR_UNSUPPORTED;
   if (!aligned(d->cache, 16)) return TQ_ERR_MISALIGNED;
@@ -114,6 +136,10 @@ tq_status verify_args(const tq_cache_desc* cache, const void* q, const int32_t* 
   a.dv = nullptr;
   a.cache_w = nullptr;
   a.plain_norm = cache->preset == TQ_PRESET_K3V4 ? 1 : 0;
+  {
+    const SignMask m = rs_signs(cache->preset);
+    for (int i = 0; i < 4; ++i) a.signs[i] = m.w[i];
+  }
   a.cb = codebook();
   return TQ_OK;
 }
@@ -131,8 +157,7 @@ size_t tq_partials_bytes(int32_t n_spec, int32_t B, int32_t Hq, int32_t num_kv_s
 
 tq_status tq_codebook(int32_t preset, float* centroids_out) {
   if (!centroids_out) return TQ_ERR_INVALID_ARG;
-  if (preset != TQ_PRESET_K3V4_NC && preset != TQ_PRESET_K3V4)
-    return preset == TQ_PRESET_K8V4 ? TQ_ERR_UNSUPPORTED : TQ_ERR_INVALID_ARG;
+  if (!is_k3(preset)) return preset == TQ_PRESET_K8V4 ? TQ_ERR_UNSUPPORTED : TQ_ERR_INVALID_ARG;
   const tq::Codebook& cb = codebook();
   for (int i = 0; i < 8; ++i) centroids_out[i] = __half2float(__ushort_as_half(cb.c[i]));
   return TQ_OK;
@@ -171,6 +196,11 @@ tq_status tq_store(const tq_cache_desc* cache, const void* k, const void* v, con
   a.max_blocks = 0;
   a.seq_lens = nullptr;
   a.n_spec = 0;
+  a.plain_norm = cache->preset == TQ_PRESET_K3V4 ? 1 : 0;
+  {
+    const SignMask m = rs_signs(cache->preset);
+    for (int i = 0; i < 4; ++i) a.signs[i] = m.w[i];
+  }
   a.cb = codebook();
   return from_cuda(tq::launch_store(cache->preset, a, static_cast<cudaStream_t>(stream)));
 }
@@ -244,6 +274,8 @@ tq_status tq_store_verify(const tq_cache_desc* cache, const void* k_new, const v
   sa.max_blocks = max_blocks;
   sa.seq_lens = seq_lens;
   sa.n_spec = n_spec;
+  sa.plain_norm = a.plain_norm;
+  for (int i = 0; i < 4; ++i) sa.signs[i] = a.signs[i];
   sa.cb = codebook();
   s = from_cuda(tq::launch_store(cache->preset, sa, st));
   if (s != TQ_OK) return s;

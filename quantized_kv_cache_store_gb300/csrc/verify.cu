@@ -170,6 +170,11 @@ __global__ void __launch_bounds__(RW* TW * 32, 1) verify_stage1_kernel(VerifyArg
       x[3] = __high2float(h1);
     }
     if (PRESET == 1) {
+      // k3v4_nc_rs: q_rot = H diag(s) q / sqrt(128)
+      const uint32_t sg = (a.signs[lane >> 3] >> (4 * (lane & 7))) & 0xFu;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if ((sg >> i) & 1u) x[i] = -x[i];
       float u = x[0], v = x[1];
       x[0] = u + v;
       x[1] = u - v;

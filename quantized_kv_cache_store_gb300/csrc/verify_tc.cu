@@ -414,6 +414,13 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         }
       }
       if (PRESET == 1) {
+        // k3v4_nc_rs: q_rot = H diag(s) q / sqrt(128), signs of coordinates 16 part + e
+        const uint32_t sg = (a.signs[part >> 1] >> (16 * (part & 1))) & 0xFFFFu;
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          if ((sg >> e) & 1u) x[e] = -x[e];
+      }
+      if (PRESET == 1) {
 #pragma unroll
         for (int hs = 1; hs < 16; hs <<= 1)
 #pragma unroll
@@ -687,7 +694,8 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
                                   (uint16_t)(kr.y >> 16)};
           const uint16_t vh[4] = {(uint16_t)(vr.x & 0xFFFF), (uint16_t)(vr.x >> 16), (uint16_t)(vr.y & 0xFFFF),
                                   (uint16_t)(vr.y >> 16)};
-          store_ops::store_token<PRESET>(page, pos % kBlock, lane, kh, vh, a.cb, a.plain_norm != 0);
+          store_ops::store_token<PRESET>(page, pos % kBlock, lane, kh, vh, a.cb, a.plain_norm != 0,
+                                         store_ops::lane_signs(a.signs, lane));
         }
         // the pages' new bytes, written through the generic proxy, are read next by bulk copies
         asm volatile("fence.proxy.async.global;\n" ::: "memory");

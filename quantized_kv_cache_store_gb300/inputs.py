@@ -27,13 +27,13 @@ import torch
 
 HEAD_DIM = 128
 BLOCK = 16
-PRESETS = {"k8v4": 0, "k3v4_nc": 1, "k3v4": 2}
+PRESETS = {"k8v4": 0, "k3v4_nc": 1, "k3v4": 2, "k3v4_nc_rs": 3}
 
 
 @dataclass(frozen=True)
 class Workload:
     name: str
-    preset: str            # "k8v4" | "k3v4_nc" | "k3v4"
+    preset: str            # "k8v4" | "k3v4_nc" | "k3v4" | "k3v4_nc_rs"
     n_spec: int
     B: int
     Hq: int

@@ -25,7 +25,9 @@ TQ_ERR_TIMEOUT = 5
 TQ_PRESET_K8V4 = 0
 TQ_PRESET_K3V4_NC = 1
 TQ_PRESET_K3V4 = 2
-PRESETS = {"k8v4": TQ_PRESET_K8V4, "k3v4_nc": TQ_PRESET_K3V4_NC, "k3v4": TQ_PRESET_K3V4}
+TQ_PRESET_K3V4_NC_RS = 3
+PRESETS = {"k8v4": TQ_PRESET_K8V4, "k3v4_nc": TQ_PRESET_K3V4_NC, "k3v4": TQ_PRESET_K3V4,
+           "k3v4_nc_rs": TQ_PRESET_K3V4_NC_RS}
 
 _lock = threading.Lock()
 _lib = None

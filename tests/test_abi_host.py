@@ -35,6 +35,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_page_and_partials_bytes(lib):
     assert tqkv.tq_page_bytes(0) == 3136 and tqkv.tq_page_bytes(1) == 1920 and tqkv.tq_page_bytes(2) == 1920
+    assert tqkv.tq_page_bytes(3) == 1920
     assert tqkv.tq_page_bytes(7) == 0
     assert tqkv.tq_partials_bytes(8, 4, 32, 8) == 8 * 4 * 32 * 8 * 129 * 4
     assert tqkv.tq_partials_bytes(0, 4, 32, 8) == 0

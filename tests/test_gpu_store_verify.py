@@ -22,6 +22,7 @@ CASES = [
     ("tiny_k8v4", {}),                                                   # drafts in chunk 0 of split 1
     ("tiny_k8v4", dict(preset="k3v4_nc")),
     ("tiny_k8v4", dict(preset="k3v4", n_spec=8, B=2, Hq=16, Hk=2, seq_len=500, num_kv_splits=3)),
+    ("tiny_k8v4", dict(preset="k3v4_nc_rs", n_spec=8, B=2, Hq=16, Hk=2, seq_len=333, num_kv_splits=2)),
     ("tiny_k8v4", dict(n_spec=16, B=1, Hq=4, Hk=1, seq_len=200, num_kv_splits=4)),  # drafts across two splits
     ("tiny_k8v4", dict(preset="k3v4_nc", n_spec=8, B=2, Hq=4, Hk=2, seq_len=203, num_kv_splits=3, causal=False)),
     ("tiny_k8v4", dict(preset="k3v4_nc", n_spec=1, B=5, Hq=32, Hk=8, seq_len=0, len_range=(1, 900),

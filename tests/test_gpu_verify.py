@@ -40,6 +40,8 @@ SMALL = [
     ("k8v4", 4, 2, 8, 1, 300, 3, True),     # 32 rows per kv-head
     ("k3v4", 8, 2, 4, 2, 203, 3, True),     # plain-norm preset
     ("k3v4", 1, 3, 8, 2, (17, 300), 4, False),
+    ("k3v4_nc_rs", 8, 2, 4, 2, 203, 3, True),  # randomised-sign Hadamard
+    ("k3v4_nc_rs", 16, 1, 8, 1, 100, 5, True),  # 128 rows: the mma.sync stage 1
     ("k3v4_nc", 2, 1, 16, 1, 77, 2, True),
     ("k3v4_nc", 16, 1, 16, 2, 190, 3, True),  # 128 rows per kv-head
 ]
@@ -261,6 +263,7 @@ FUSED = [
     ("k8v4", 3, 2, 2, 2, 3, 5, True),       # splits mostly empty
     ("k3v4_nc", 2, 1, 16, 1, 77, 16, True),
     ("k3v4", 8, 1, 8, 1, 256, 4, True),
+    ("k3v4_nc_rs", 8, 1, 32, 4, 555, 7, True),
     ("k8v4", 1, 2, 8, 1, 2000, 32, True),   # the most splits one launch merges
     ("k8v4", 2, 3, 8, 4, 700, 40, False),   # more splits than one launch merges: two launches
     ("k8v4", 16, 1, 8, 1, 100, 3, True),    # 128 rows: mma.sync stage 1 + stage 2

@@ -140,6 +140,41 @@ def test_plain_norm_preset_differs_only_in_the_factor(oracle_lib):
             assert abs(np.linalg.norm(O.decode_key(2, ppl, 0)) - fac * chat) <= 1e-12 * fac * chat
 
 
+def test_splitmix64_published_outputs(oracle_lib):
+    """The sign generator is SplitMix64: its first outputs for seed 0 are the
+    generator's published reference values."""
+    O = oracle_lib
+    assert O.splitmix64(0, 0) == 0xE220A8397B1DCDAF
+    assert O.splitmix64(0, 1) == 0x6E789E6AA1B965F4
+    s = O.rs_signs()
+    assert set(np.unique(s)) == {-1, 1} and 40 < (s < 0).sum() < 88  # a Rademacher-like vector
+    seed = 0x54515F5349474E53
+    assert all((s[j] < 0) == bool(O.splitmix64(seed, j) >> 63) for j in range(128))
+
+
+def test_signed_rotation_round_trips_centroid_vectors(oracle_lib):
+    """Preset k3v4_nc_rs rotates by H diag(s): a key built as s * (H c) from a
+    centroid vector c codes back to c exactly, decodes to the key itself, and
+    the unsigned preset does not recover c from it."""
+    O = oracle_lib
+    rng = np.random.default_rng(15)
+    cb = O.codebook16().view(np.float16).astype(np.float64)
+    bnd = (cb[:-1] + cb[1:]) / 2
+    s = O.rs_signs().astype(np.float64)
+    for _ in range(10):
+        y = rng.standard_normal(D) / np.sqrt(D)
+        idx = np.searchsorted(bnd, y, side="left").astype(np.uint8)
+        c = cb[idx]
+        kk = 2.0 * s * (_H() @ c)
+        k = kk.astype(np.float16)
+        page = _one_token_page(O, 3, k, np.zeros(D, np.float16))
+        assert np.array_equal(O.unpack3(page[0:48]), idx)
+        kh = O.decode_key(3, page, 0)  # = nc s (H c) / sqrt(D): the key up to fp16 rounding
+        assert np.max(np.abs(kh - kk)) <= 2.0 ** -9 * np.max(np.abs(kk))
+        plain = _one_token_page(O, 1, k, np.zeros(D, np.float16))
+        assert not np.array_equal(O.unpack3(plain[0:48]), idx)
+
+
 def test_key3_distortion_matches_lloyd_max(oracle_lib):
     """Mean relative squared error of norm-corrected 3-bit keys: with
     distortion d = 0.03454 of the unit-Gaussian Lloyd-Max quantiser, the
