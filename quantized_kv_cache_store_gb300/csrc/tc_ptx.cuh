@@ -57,16 +57,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                : "memory");
 }
 
-// shared -> global bulk copy (bulk-group completion); both addresses 16-byte
-// aligned, bytes a multiple of 16
-__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
-// every committed bulk group of this thread has completed (writes performed)
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
-
 // tiled tensor copy (TMA), 3-D box at coordinates {x, y, z}; completes tx on `bar`
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar) {
   asm volatile(
@@ -120,15 +110,8 @@ __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sy
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar) : "memory");
 }
-// D(tmem) (+)= A(tmem) * B(smem descriptor), kind::f16, fp32 accumulate
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
-      "r"(a), "l"(bdesc), "r"(idesc), "r"(accum)
-      : "memory");
-}
-
-// Eight MMAs D (+)= A_k * B_k, k = 0..7, into the same accumulator, issued
+// Eight MMAs D (+)= A_k * B_k (kind::f16, A in tensor memory, B by shared-
+// memory descriptor, fp32 accumulate), k = 0..7, into the same accumulator, issued
 // back to back: A_k at tensor-memory column a + 8 k, B_k's descriptor =
 // bdesc + boff[k] (start-address units of 16 bytes).  The first MMA
 // accumulates iff acc0; the others always do.
