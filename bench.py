@@ -564,8 +564,10 @@ def run_reference(args):
            "scaling": "weak", "vs_baseline": None, "dtype": "fp32 encoder / fp64 attention",
            "data": "synthetic (same seeded workload as the GPU arm)",
            "config": {"workload": wl.name, "preset": wl.preset, "n_spec": wl.n_spec, "B": wl.B, "Hq": wl.Hq,
-                      "Hk": wl.Hk, "D": 128, "seq_len": wl.seq_len, "causal": wl.causal,
-                      "step": "oracle store of the drafts + fp64 verify of all rows"},
+                      "Hk": wl.Hk, "D": 128, "seq_len": wl.seq_len, "cached_len": wl.seq_len - wl.n_spec,
+                      "causal": wl.causal, "num_kv_splits": wl.num_kv_splits,
+                      "seed": 1000 + CONFIG_INDEX[args.workload],
+                      "step": "oracle store of the drafts + fp64 verify of all rows (split-free)"},
            "cpu_baseline": {"value": round(v, 1), "unit": "us", "cores": cores, "kind": "oracle",
                             "sample": f"{k} full oracle calls (steps capped from {args.steps} to fit "
                                       f"{budget:.0f} s), OpenMP {cores} threads"},
