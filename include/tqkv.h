@@ -181,7 +181,9 @@ tq_status tq_verify_stage2(const float* partial_o, const float* partial_lse, int
  *            overlap in time (order them on one stream);
  *   out      fp32 [n_spec][B][Hq][128], 16-byte aligned; written.
  * A cross-split wait that expires writes NaN rows and sets the device error
- * word (tq_device_status). */
+ * word (tq_device_status); the counters may then be left non-zero, so after
+ * a call that set the error word the caller zeroes tickets again before the
+ * next call. */
 tq_status tq_verify(const tq_cache_desc* cache, const void* q, const int32_t* block_table,
                     int32_t max_blocks, const int32_t* seq_lens, int32_t n_spec, int32_t B,
                     int32_t Hq, int32_t num_kv_splits, int32_t causal, float* partial_o,
@@ -214,7 +216,10 @@ tq_status tq_store_verify(const tq_cache_desc* cache, const void* k_new, const v
  * tq_verify without partial_o, partial_lse and tickets.
  *   Set-up: the first call on a device looks up the arrays' addresses and
  *     clears the counters, synchronising the device; make it before any
- *     stream capture on that device.
+ *     stream capture on that device.  After tq_device_status has reported an
+ *     expired wait, the next call on every device sets the scratch up again
+ *     (the counters may have been left non-zero), so that call too must come
+ *     before any capture.
  *   Sharing: every call on a device uses the same scratch.  Calls on one
  *     device must not overlap in time (order them on one stream); calls that
  *     run concurrently on different streams race on the scratch.

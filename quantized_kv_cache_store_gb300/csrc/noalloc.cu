@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "../../include/tqkv.h"
+#include "tq_common.cuh"
 
 namespace {
 
@@ -61,6 +62,11 @@ tq_status device_scratch(DeviceScratch* out) {
 }
 
 }  // namespace
+
+void tq::noalloc_mark_stale() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (DeviceScratch& d : g_dev) d.ready = false;
+}
 
 extern "C" tq_status tq_verify_noalloc(const tq_cache_desc* cache, const void* q, const int32_t* block_table,
                                        int32_t max_blocks, const int32_t* seq_lens, int32_t n_spec, int32_t B,

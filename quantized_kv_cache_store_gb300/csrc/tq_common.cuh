@@ -130,5 +130,8 @@ bool verify_fused_supported(int preset, const VerifyArgs& a);
 cudaError_t launch_verify_fused(int preset, const VerifyArgs& a, cudaStream_t st);
 // sticky device-side error word (nonzero after a bounded wait expired)
 cudaError_t read_device_error(unsigned int* out, bool clear);
+// after an expired wait the merge counters of tq_verify_noalloc's scratch may
+// be left non-zero: its next call on every device sets the scratch up again
+void noalloc_mark_stale();
 
 }  // namespace tq

@@ -302,6 +302,7 @@ tq_status tq_verify_stage2(const float* partial_o, const float* partial_lse, int
 tq_status tq_device_status(void) {
   unsigned int word = 0;
   if (tq::read_device_error(&word, true) != cudaSuccess) return TQ_ERR_CUDA;
+  if (word) tq::noalloc_mark_stale();
   return word ? TQ_ERR_TIMEOUT : TQ_OK;
 }
 
