@@ -23,7 +23,10 @@
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers into caller-owned memory; the
- *     library never allocates, frees, synchronises or keeps per-call state.
+ *     library never allocates, frees or keeps per-call state, and only
+ *     tq_device_status and the set-up of tq_verify_noalloc synchronise (the
+ *     sticky error word and tq_verify_noalloc's scratch are the library's
+ *     only device state).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *     only enqueued; results are ready when the stream reaches that point.
  *   - Arguments are validated on the host before anything is launched.  On
