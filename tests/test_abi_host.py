@@ -142,3 +142,18 @@ def test_store_verify_validation(lib):
     assert v(t=FAKE + 2) == tqkv.TQ_ERR_MISALIGNED
     assert v(q=0) == tqkv.TQ_ERR_INVALID_ARG
     assert v(B=0) == tqkv.TQ_OK  # nothing to enqueue
+
+
+def test_header_enums_match_the_binding():
+    """The preset and status values the header declares are the binding's and
+    the input recipe's."""
+    from quantized_kv_cache_store_gb300 import inputs
+
+    text = open(HEADER).read()
+    decl = {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(TQ_[A-Z0-9_]+)\s*=\s*(\d+)", text)}
+    for name in ("TQ_OK", "TQ_ERR_INVALID_ARG", "TQ_ERR_UNSUPPORTED", "TQ_ERR_MISALIGNED", "TQ_ERR_CUDA",
+                 "TQ_ERR_TIMEOUT", "TQ_PRESET_K8V4", "TQ_PRESET_K3V4_NC", "TQ_PRESET_K3V4", "TQ_PRESET_K3V4_NC_RS"):
+        assert decl[name] == getattr(tqkv, name), name
+    assert tqkv.PRESETS == inputs.PRESETS
+    for preset in tqkv.PRESETS.values():
+        assert tqkv.tq_page_bytes(preset) > 0
