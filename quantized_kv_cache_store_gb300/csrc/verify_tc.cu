@@ -68,10 +68,14 @@ constexpr float kLn2 = 0.6931471805599453f;
 // a bounded wait gives up after kWaitTries tests of up to kSuspendNs each (~1 s)
 constexpr uint32_t kWaitTries = 50000;
 constexpr uint32_t kSuspendNs = 20000;
-// the cross-CTA wait of the single-launch verify gives up after kSpinTries
-// polls (a poll is an L2 round trip plus a 64 ns sleep: well over 100 ms)
-constexpr uint32_t kSpinTries = 1u << 20;
+// the cross-CTA waits of the single-launch verify give up after kSpinNs of
+// polling (or kSpinTries polls, should the timer not advance)
+constexpr uint64_t kSpinNs = 500000000ull;
+constexpr uint32_t kSpinTries = 1u << 24;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
+// the MMA issuer polls its barriers without blocking; it gives up after
+// kSpinNs without progress (or kIssuerPolls idle polls)
+constexpr uint32_t kIssuerPolls = 1u << 26;
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -86,17 +90,19 @@ struct Cfg {
   static constexpr int kRestBytes = L::kPage - kKeyBlock;
   static constexpr int kRestOff = kPages * kKeyBlock;
   static constexpr int kStageBytes = align_up(kPages * L::kPage, 1024);
-  static constexpr int kStages = PRESET == 0 ? 4 : 6;
+  static constexpr int kStages = PRESET == 0 ? 5 : 8;
   static constexpr int kSW = NR == 64 ? 2 : 1;    // softmax warpgroups
   static constexpr int kRS = NR == 64 ? 32 : NR;  // query rows per softmax thread
   static constexpr int kThreads = 256 + 128 * kSW;
   // per-thread register budgets after setmaxnreg (control / dequant /
   // softmax); their sum must stay within what the launch granted (checked at
   // launch: 128 registers a thread for 512 threads, 168 for 384)
-  static constexpr int kRegCtl = kSW == 2 ? 40 : 32;
+  // (setmaxnreg is executed by all four warps of a warpgroup together)
+  static constexpr int kRegCtl = kSW == 2 ? 40 : 48;
   static constexpr int kRegDq = 96;
   static constexpr int kRegSm = kSW == 2 ? 184 : 232;
   static constexpr int kRegNeeded = 128 * kRegCtl + 128 * kRegDq + 128 * kSW * kRegSm;
+  static_assert(kRegNeeded <= 65536, "register split exceeds the register file");
   static constexpr int kLine = 2 * NR;  // bytes of one P' line (one token)
   static constexpr int kSwzBits = NR == 64 ? 3 : (NR == 32 ? 2 : 1);
   static constexpr uint32_t kSwzMode = NR == 64 ? 2u : (NR == 32 ? 4u : 6u);
@@ -107,19 +113,19 @@ struct Cfg {
   static constexpr int kP = kQ + align_up(kQBytes, 1024);
   static constexpr int kPBytes = kTok * kLine;  // one buffer
   static constexpr int kCol = kP + 3 * kPBytes;  // float4 [4][128]: score scale, P' scale, v zero, first row
-  // per softmax warpgroup: -m [32], rescale factors [32], row constants [32][2], lse [32]
+  // per softmax warpgroup (floats): -m [32] @0, rescale factors [32] @32,
+  // row constants float2 [32] @64, per-warp row maxima [4][32] @128, per-warp
+  // row sums of l and of the zero term [2][128] @256, rows without a maximum
+  // yet (bit mask) @512
   static constexpr int kRed = kCol + 4 * kTok * 16;
-  static constexpr int kRedWG = 160 * 4;
-  // per softmax warpgroup: float [32 rows][128 tokens or coordinates] for transposes
-  static constexpr int kScr = kRed + kSW * kRedWG;
-  static constexpr int kScrWG = kRS * 128 * 4;
-  static constexpr int kPair = kScr + kSW * kScrWG;  // u32 [64][32] (k3v4_nc)
+  static constexpr int kRedWG = 4096;
+  static constexpr int kPair = kRed + kSW * kRedWG;  // u32 [64][32] (k3v4_nc)
   static constexpr int kPValid = kPair + (PRESET == 1 ? 64 * 32 * 4 : 0);  // u8 [kStages][8]
   static constexpr int kBar = align_up(kPValid + kStages * 8, 8);
-  // full[kStages] empty[kStages] ak[4] sready[2] pfull[3] pv[3] sfree[2] av[3] dstored
+  // full[kStages] empty[kStages] ak[4] sready[2] pfull[3] pv[3] sfree[2] av[3]
   static constexpr int kProducers = 3;  // warps 0, 2, 3 copy pages 0-2, 3-5, 6-7 of a chunk
-  static constexpr int kNumBars = 2 * kStages + 18;
-  static constexpr int kMisc = kBar + 8 * kNumBars;  // u32 tmem base, u32 abort
+  static constexpr int kNumBars = 2 * kStages + 17;
+  static constexpr int kMisc = kBar + 8 * kNumBars;  // u32 tmem base, u32 abort, u32 merge go
   static constexpr int kSmem = kMisc + 16 + 1024;    // + alignment slack
   // tensor memory columns
   static constexpr uint32_t kTmemCols = 512;
@@ -149,18 +155,29 @@ struct Bars {
   __device__ uint32_t pv(int i) const { return base + 8 * (2 * stages + 9 + i); }     // O^T += V^T P'^T done (c % 3)
   __device__ uint32_t sfree(int b) const { return base + 8 * (2 * stages + 12 + b); } // S^T(c) read by the softmax (c % 2)
   __device__ uint32_t av(int i) const { return base + 8 * (2 * stages + 14 + i); }    // A_V written (c % 3)
-  __device__ uint32_t dstored() const { return base + 8 * (2 * stages + 17); }        // drafts written (once)
 };
+
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 // Bounded wait for a global counter written by other CTAs of the same
 // (cooperative, hence co-resident) grid to reach target; false when it
-// expired, which is recorded in the device error word.
+// expired (after kSpinNs), which is recorded in the device error word.
 __device__ __forceinline__ bool spin_until_at_least(const uint32_t* counter, uint32_t target) {
-  for (uint32_t i = 0; i < kSpinTries; ++i) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
     if (v >= target) return true;
-    __nanosleep(64);
+    if ((i & 63) == 0) {
+      const uint64_t t = now_ns();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > kSpinNs || i >= kSpinTries) break;
+    }
+    if (i >= 256) __nanosleep(64);
   }
   atomicOr(&g_tq_device_error, 1u);
   return false;
@@ -239,19 +256,6 @@ __device__ __forceinline__ void warp_transpose_reduce(float (&v)[NC], int lane) 
   }
 }
 
-// Transposes through shared memory ([32 rows][128 tokens] of floats): token t
-// of row k sits in 16-byte slot ((t / 4) % 8) ^ (4 (k % 2) + t / 32) of the
-// row's quarter t / 32, so that writes of one row by 32 consecutive tokens and
-// reads of row segments (thread -> row i / 4, quarter i % 4) are both free of
-// bank conflicts.
-__device__ __forceinline__ int tr_index(int k, int t) {
-  const int qt = t >> 5;
-  return k * 128 + 32 * qt + 4 * (((t >> 2) & 7) ^ (4 * (k & 1) + qt)) + (t & 3);
-}
-__device__ __forceinline__ const float4* tr_seg(const float* base, int k, int qt, int u) {
-  return reinterpret_cast<const float4*>(base + k * 128 + 32 * qt + 4 * (u ^ (4 * (k & 1) + qt)));
-}
-
 // Position of chunk token t on the K axis of the P.V contraction.  Within
 // each group of 8 tokens the value operand holds the pairs (0,5) (1,4) (2,7)
 // (3,6), the order the nibble masks produce.
@@ -298,13 +302,16 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
   const int page_lo = t_lo / kBlock;
   const int npages = t_hi > t_lo ? (t_hi - t_lo + kBlock - 1) / kBlock : 0;
   const int nchunks = (npages + C::kPages - 1) / C::kPages;
-  // single-launch store + verify: this split first stores the drafts at
-  // positions [d_lo, t_hi) (the drafts sit at [L_b - n_spec, L_b), and the
-  // splits are page-aligned, so no other CTA reads their pages); chunks from
-  // c_draft on are copied only after that
+  // single-launch store + verify: the drafts sit at [L_b - n_spec, L_b);
+  // the S splits of the pair store them (split s: drafts n = s mod S, on
+  // producer warp 3 while the first pages are on their way) and count them
+  // on the pair's draft counter; a split whose range holds drafts copies the
+  // chunks from c_draft on only once all n_spec are counted
+  const bool drafts = FUSED && a.dk != nullptr;
   const int d_lo = max(max(L_b - a.n_spec, t_lo), 0);
-  const bool stores = FUSED && a.dk != nullptr && d_lo < t_hi;
-  const int c_draft = stores ? (d_lo - t_lo) / (C::kPages * kBlock) : nchunks;
+  const bool reads_drafts = drafts && d_lo < t_hi;
+  const int c_draft = reads_drafts ? (d_lo - t_lo) / (C::kPages * kBlock) : nchunks;
+  uint32_t* pair_tickets = FUSED ? a.tickets + ((long)b * a.Hk + kvh) * 4 : nullptr;
   const int32_t* bt = a.block_table + (long)b * a.max_blocks;
 
   // Producers = warps 0, 2, 3 (C::kProducers): producer w copies pages
@@ -324,6 +331,8 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     }
     return id;
   };
+  // the cache pages are read once per call: evict them from L2 first
+  const uint64_t pol = producer ? l2_evict_first() : 0ull;
   auto produce = [&](int c) {
     const int st = c % C::kStages;
     const int mine = __shfl_sync(kFull, ids, (c & 3) * C::kPages + (lane & 7));
@@ -339,10 +348,10 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       const long page = (long)mine * a.Hk + kvh;
       const uint8_t* src = a.cache + page * L::kPage;
       if constexpr (PRESET == 0) {
-        tma_load_3d(dst + lane * C::kKeyBlock, &tmap_keys, 0, 0, (int)page, bars.full(st));
-        bulk_g2s(dst + C::kRestOff + lane * C::kRestBytes, src + C::kKeyBlock, C::kRestBytes, bars.full(st));
+        tma_load_3d_hint(dst + lane * C::kKeyBlock, &tmap_keys, 0, 0, (int)page, bars.full(st), pol);
+        bulk_g2s_hint(dst + C::kRestOff + lane * C::kRestBytes, src + C::kKeyBlock, C::kRestBytes, bars.full(st), pol);
       } else {
-        bulk_g2s(dst + lane * L::kPage, src, L::kPage, bars.full(st));
+        bulk_g2s_hint(dst + lane * L::kPage, src, L::kPage, bars.full(st), pol);
       }
     }
     __syncwarp();
@@ -369,7 +378,6 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       mbar_init(bars.sready(i), 5);
       mbar_init(bars.sfree(i), 4 * C::kSW);
     }
-    mbar_init(bars.dstored(), 4 * C::kSW);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -379,10 +387,10 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
   }
   cta_bar();  // barriers initialised
 
-  // the first kStages chunks need no free slot: issue them before the prologue
-  // only chunk 0 goes out before the prologue: with every CTA streaming its
-  // whole ring at once the first chunk would land last
-  const int prefill = c_draft == 0 ? 0 : min(nchunks, 1);
+  // the whole ring goes out at once (up to the chunk holding drafts this
+  // split stores first); the first chunk lands about as early as when it
+  // is requested alone
+  const int prefill = min(min(nchunks, C::kStages), min(c_draft, 4));
   if (producer)
     for (int c = 0; c < prefill; ++c) produce(c);
 
@@ -468,6 +476,40 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
   if (warp < 4) {
     regs_dec<C::kRegCtl>();
     if (producer) {
+      if constexpr (FUSED) {
+        if (warp == 3 && drafts) {
+          // ================= the drafts n = split mod S of this pair, between
+          // the first chunks' copies and the next ones (this warp's copies of
+          // chunk prefill wait for a free ring stage anyway); skipped drafts
+          // (no position, invalid block) count too
+          uint32_t count = 0;
+          for (int n = split; n < a.n_spec; n += a.S) {
+            ++count;
+            const int pos = L_b - a.n_spec + n;
+            if (pos < 0) continue;
+            const int id = a.block_table[(long)b * a.max_blocks + pos / kBlock];
+            if (id < 0 || id >= a.num_blocks) continue;
+            uint8_t* page = a.cache_w + ((long)id * a.Hk + kvh) * L::kPage;
+            const long base = (((long)b * a.n_spec + n) * a.Hk + kvh) * kD + 4 * lane;
+            const uint2 kr = *reinterpret_cast<const uint2*>(a.dk + base);
+            const uint2 vr = *reinterpret_cast<const uint2*>(a.dv + base);
+            const uint16_t kh[4] = {(uint16_t)(kr.x & 0xFFFF), (uint16_t)(kr.x >> 16), (uint16_t)(kr.y & 0xFFFF),
+                                    (uint16_t)(kr.y >> 16)};
+            const uint16_t vh[4] = {(uint16_t)(vr.x & 0xFFFF), (uint16_t)(vr.x >> 16), (uint16_t)(vr.y & 0xFFFF),
+                                    (uint16_t)(vr.y >> 16)};
+            store_ops::store_token<PRESET>(page, pos % kBlock, lane, kh, vh, a.cb, a.plain_norm != 0,
+                                           store_ops::lane_signs(a.signs, lane));
+          }
+          if (count > 0) {
+            // the pages' new bytes (generic proxy) are read next by bulk copies
+            // of this or another CTA: proxy fence, then a release at gpu scope
+            asm volatile("fence.proxy.async.global;\n" ::: "memory");
+            __syncwarp();
+            if (lane == 0)
+              asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(pair_tickets + 2), "r"(count) : "memory");
+          }
+        }
+      }
       // ================= producers: their pages of each chunk into the ring
       int c = prefill;
       for (; c < nchunks; ++c) {
@@ -475,19 +517,34 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
           ids = ids_next;
           ids_next = fetch_ids(c + 4);  // lands while this group is copied
         }
-        if (!wait_bar(bars.empty(c % C::kStages), ((c / C::kStages) - 1) & 1, abort_flag)) break;
-        if (c == c_draft && !wait_bar(bars.dstored(), 0, abort_flag)) break;
+        if (c >= C::kStages && !wait_bar(bars.empty(c % C::kStages), ((c / C::kStages) - 1) & 1, abort_flag)) break;
+        if (c == c_draft) {
+          // every draft of the pair is stored (by whichever split): the
+          // generic-proxy writes of other CTAs, acquired here, precede the
+          // bulk copies of this warp
+          bool ok = true;
+          if (lane == 0) ok = spin_until_at_least(pair_tickets + 2, (uint32_t)a.n_spec);
+          ok = __shfl_sync(kFull, ok, 0);
+          if (!ok) {
+            *abort_flag = 1u;
+            break;
+          }
+          asm volatile("fence.proxy.async.global;\n" ::: "memory");
+        }
         produce(c);
       }
       // drain: copies still in flight must land before the CTA can exit
       for (int cc = max(0, c - C::kStages); cc < c; ++cc)
         wait_bar(bars.full(cc % C::kStages), (cc / C::kStages) & 1, abort_flag, false);
     } else if (warp == 1) {
-      // ================= MMA issuer (one thread), in the order P.V(c - 3),
-      // S^T(c): P.V(c - 3) waits for softmax(c - 3), S^T(c) for softmax(c - 2)
-      // to release its buffer, so neither waits behind the other.  Since a
-      // commit tracks every earlier MMA of this thread, sready(c) also means
-      // that P.V(c - 3) is done: P' buffer c % 3 and A_V buffer c % 3 are free.
+      // ================= MMA issuer (one thread), never blocked on one
+      // operand while the other kind of MMA could go: S^T(c) = K_hat(c) Q^T
+      // once softmax(c - 2) released its buffer and the keys of chunk c are in
+      // tensor memory; O^T += V^T P'^T(c) once softmax(c) wrote P'(c) and the
+      // values of chunk c are in tensor memory.  S^T(c) is issued only after
+      // P.V(c - 3): a commit tracks every earlier MMA of this thread, so the
+      // completion of S^T(c) then also means that P.V(c - 3) is done, which
+      // frees P' buffer c % 3 and value buffer c % 3 without a wait of their own.
       if (lane == 0) {
         constexpr uint32_t id_qk = idesc_f16(128, NR, 0, 0);
         constexpr uint32_t id_pv = idesc_f16(128, NR, 0, 1);
@@ -495,39 +552,53 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         constexpr uint32_t kL = C::kLine;  // P' line bytes: 16 lines per K-step
         const uint64_t q_desc = smem_desc(sbase + C::kQ, 16, 1024, 2);
         const uint64_t p_desc = smem_desc(sbase + C::kP, 16, 8 * C::kLine, C::kSwzMode);
-        auto issue_qk = [&](int c) -> bool {
-          if (c >= 2 && !wait_bar(bars.sfree(c & 1), ((c - 2) >> 1) & 1, abort_flag)) return false;
-          if (!wait_bar(bars.ak(c & 3), (c >> 2) & 1, abort_flag)) return false;
-          tc_fence_after();
-          mma_ts_x8<2, 4, 6, kQ1, kQ1 + 2, kQ1 + 4, kQ1 + 6>(tmem + C::kTS + NR * (c & 1), tmem + C::kTAK + 64 * (c & 1),
-                                                             q_desc, id_qk, 0u);
-          tc_commit(bars.sready(c & 1));
-          return true;
-        };
-        auto issue_pv = [&](int c) -> bool {
-          if (!wait_bar(bars.pfull(c % 3), (c / 3) & 1, abort_flag) || !wait_bar(bars.av(c % 3), (c / 3) & 1, abort_flag))
-            return false;
-          tc_fence_after();
-          mma_ts_x8<kL, 2 * kL, 3 * kL, 4 * kL, 5 * kL, 6 * kL, 7 * kL>(
-              tmem + C::kTO, tmem + C::kTAV + 64 * (c % 3), p_desc + (uint64_t)(((c % 3) * C::kPBytes) >> 4), id_pv,
-              c > 0 ? 1u : 0u);
-          tc_commit(bars.pv(c % 3));
-          return true;
-        };
-        int done_qk = 0, done_pv = 0;
-        for (int c = 0; c < nchunks + 3; ++c) {
-          if (c >= 3) {
-            if (!issue_pv(c - 3)) break;
-            ++done_pv;
+        int nq = 0, np = 0;
+        uint32_t idle = 0;
+        uint64_t idle_since = 0;  // time of the first idle poll since the last issue
+        while (np < nchunks) {
+          bool did = false;
+          if (nq < nchunks && nq - 3 < np &&
+              (nq < 2 || mbar_test_wait(bars.sfree(nq & 1), ((nq - 2) >> 1) & 1)) &&
+              mbar_test_wait(bars.ak(nq & 3), (nq >> 2) & 1)) {
+            tc_fence_after();
+            mma_ts_x8<2, 4, 6, kQ1, kQ1 + 2, kQ1 + 4, kQ1 + 6>(tmem + C::kTS + NR * (nq & 1),
+                                                               tmem + C::kTAK + 64 * (nq & 1), q_desc, id_qk, 0u);
+            tc_commit(bars.sready(nq & 1));
+            ++nq;
+            did = true;
           }
-          if (c < nchunks) {
-            if (!issue_qk(c)) break;
-            ++done_qk;
+          if (np < nq && mbar_test_wait(bars.pfull(np % 3), (np / 3) & 1) &&
+              mbar_test_wait(bars.av(np % 3), (np / 3) & 1)) {
+            tc_fence_after();
+            mma_ts_x8<kL, 2 * kL, 3 * kL, 4 * kL, 5 * kL, 6 * kL, 7 * kL>(
+                tmem + C::kTO, tmem + C::kTAV + 64 * (np % 3), p_desc + (uint64_t)(((np % 3) * C::kPBytes) >> 4),
+                id_pv, np > 0 ? 1u : 0u);
+            tc_commit(bars.pv(np % 3));
+            ++np;
+            did = true;
+          }
+          if (!did) {
+            if (*abort_flag) break;
+            ++idle;
+            if ((idle & 63) == 0) {
+              const uint64_t t = now_ns();
+              if (idle_since == 0) {
+                idle_since = t;
+              } else if (t - idle_since > kSpinNs || idle > kIssuerPolls) {
+                *abort_flag = 1u;
+                atomicOr(&g_tq_device_error, 1u);
+                break;
+              }
+            }
+            __nanosleep(20);
+          } else {
+            idle = 0;
+            idle_since = 0;
           }
         }
         // drain before tensor memory is freed
-        if (done_qk > 0) wait_bar(bars.sready((done_qk - 1) & 1), ((done_qk - 1) >> 1) & 1, abort_flag, false);
-        if (done_pv > 0) wait_bar(bars.pv((done_pv - 1) % 3), ((done_pv - 1) / 3) & 1, abort_flag, false);
+        if (nq > 0) wait_bar(bars.sready((nq - 1) & 1), ((nq - 1) >> 1) & 1, abort_flag, false);
+        if (np > 0) wait_bar(bars.pv((np - 1) % 3), ((np - 1) / 3) & 1, abort_flag, false);
       }
       __syncwarp();
     }
@@ -677,32 +748,6 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     }
   } else {
     regs_inc<C::kRegSm>();
-    if constexpr (FUSED) {
-      if (stores) {
-        // the drafts of this split, one warp per draft, while the first scores
-        // are still on their way; then released to the producers
-        for (int n = warp - 8; n < a.n_spec; n += 4 * C::kSW) {
-          const int pos = L_b - a.n_spec + n;
-          if (pos < d_lo || pos >= t_hi) continue;
-          const int id = a.block_table[(long)b * a.max_blocks + pos / kBlock];
-          if (id < 0 || id >= a.num_blocks) continue;
-          uint8_t* page = a.cache_w + ((long)id * a.Hk + kvh) * L::kPage;
-          const long base = (((long)b * a.n_spec + n) * a.Hk + kvh) * kD + 4 * lane;
-          const uint2 kr = *reinterpret_cast<const uint2*>(a.dk + base);
-          const uint2 vr = *reinterpret_cast<const uint2*>(a.dv + base);
-          const uint16_t kh[4] = {(uint16_t)(kr.x & 0xFFFF), (uint16_t)(kr.x >> 16), (uint16_t)(kr.y & 0xFFFF),
-                                  (uint16_t)(kr.y >> 16)};
-          const uint16_t vh[4] = {(uint16_t)(vr.x & 0xFFFF), (uint16_t)(vr.x >> 16), (uint16_t)(vr.y & 0xFFFF),
-                                  (uint16_t)(vr.y >> 16)};
-          store_ops::store_token<PRESET>(page, pos % kBlock, lane, kh, vh, a.cb, a.plain_norm != 0,
-                                         store_ops::lane_signs(a.signs, lane));
-        }
-        // the pages' new bytes, written through the generic proxy, are read next by bulk copies
-        asm volatile("fence.proxy.async.global;\n" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.dstored());
-      }
-    }
     // ================= softmax warpgroup j: thread i = TMEM lane i = token i,
     // query rows [row0, row0 + kRS)
     constexpr int kH = kRS / 2;
@@ -712,12 +757,14 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     const uint32_t lane_q = (uint32_t)(sw * 32) << 16;
     const uint32_t bar_id = 1 + j;
     const int row0 = kRS * j;
-    float* nms = reinterpret_cast<float*>(sm + C::kRed + j * C::kRedWG);  // -m per row
-    float* als = nms + 32;                                                 // rescale factor per row
-    float2* rcs = reinterpret_cast<float2*>(nms + 64);                     // (1/l * 2^24, zero term / l)
-    float* scr = reinterpret_cast<float*>(sm + C::kScr + j * C::kScrWG);  // [kRS][128]
-    // row reductions through scr: thread i sums row rr over tokens [32 qt, 32 qt + 32)
-    const int rr = i >> 2, qt = i & 3;
+    float* red = reinterpret_cast<float*>(sm + C::kRed + j * C::kRedWG);
+    float* nms = red;                                      // -m per row
+    float* als = red + 32;                                 // rescale factor per row
+    float* dlt = red + 64;                                 // m_old - m_new per row (exact path)
+    float2* rcs = reinterpret_cast<float2*>(red + 96);     // (2^24 / l, zero term / l)
+    float* wmax = red + 160;                               // [4 warps][32 rows] chunk maxima
+    float* wsum = red + 288;                               // [2][4 warps][32 rows] l, zero term
+    uint32_t* fresh = reinterpret_cast<uint32_t*>(red + 544);  // rows without a maximum yet
     // this token's line of P' (MN-major, swizzled): byte offsets of its 16-byte chunks
     uint32_t poff[kRS / 8];
     {
@@ -728,9 +775,10 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         poff[q] = lg ^ (((lg >> 7) & ((1u << C::kSwzBits) - 1u)) << 4);
       }
     }
-    // running maxima (shared by the warpgroup) start at a finite floor: the
-    // first visible score of a row always forces the exact path
-    if (i < kRS) nms[i] = 1.0e30f;
+    // m starts at 0 for every row, marked fresh: a row's first visible
+    // scores take the exact path, which sets m to their maximum
+    if (i < kRS) nms[i] = 0.f;
+    if (i == 0) *fresh = kRS == 32 ? 0xFFFFFFFFu : ((1u << kRS) - 1u);
     float2 l2[kH], z2[kH];  // l and the zero term of this token's rows (row pairs)
 #pragma unroll
     for (int k = 0; k < kH; ++k) {
@@ -753,12 +801,16 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         tmem_ld<kRS>(s_base + NR * (c & 1), x);
       }
       tc_wait_ld();
+      // S^T(c) is in registers: its buffer goes back to the MMA issuer (for S^T(c + 2))
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.sfree(c & 1));
       const float4 cp = colp[(c & 3) * 128 + i];
       const int rmin = __float_as_int(cp.w);
       const bool masked = __any_sync(kFull, rmin > row0);
       float2* d = reinterpret_cast<float2*>(x);
       // d = s * score_scale - m, masked rows -> -inf
-      auto scores = [&]() {
+      {
         const float2 cs2 = make_float2(cp.x, cp.x);
         const float4* n4 = reinterpret_cast<const float4*>(nms);
 #pragma unroll
@@ -776,8 +828,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
             if (row0 + 2 * k + 1 < rmin) d[k].y = -CUDART_INF_F;
           }
         }
-      };
-      scores();
+      }
       float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
 #pragma unroll
       for (int k = 0; k < kH; k += 2) {
@@ -786,52 +837,61 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       }
       // p = 2^d as fp16 pairs (the precision of the P' operand), issued
       // before the vote so that the vote's latency hides behind the
-      // exponentials; a vote for the exact path recomputes them
+      // exponentials; a vote for the exact path recomputes them.  The first
+      // chunk always takes the exact path (every row is fresh), without a vote.
       uint32_t ph[kH];
-      auto exps = [&]() {
+      const uint32_t fr = *fresh;
+      bool exact = c == 0;
+      if (c > 0) {
 #pragma unroll
         for (int k = 0; k < kH; ++k) ph[k] = ex2_h2(d[k].x, d[k].y);
-      };
-      exps();
-      // leave the loop together: the named barriers need all four warps
-      // S^T(c) is released to the MMA issuer (for S^T(c + 2)) once no path of
-      // this chunk reads it again
-      auto release_s = [&]() {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.sfree(c & 1));
-      };
-      if (bar_red_or(bar_id, 128, fmaxf(mx0, mx1) > kRescaleThreshold || !ok)) {
+        // exact path: some score above m + 8 (p could leave the fp16 range),
+        // or a row that has no maximum yet sees a score
+        bool need = fmaxf(mx0, mx1) > kRescaleThreshold;
+        if (fr != 0u) {
+#pragma unroll
+          for (int k = 0; k < kH; ++k) {
+            need |= ((fr >> (2 * k)) & 1u) && d[k].x > -CUDART_INF_F;
+            need |= ((fr >> (2 * k + 1)) & 1u) && d[k].y > -CUDART_INF_F;
+          }
+        }
+        // leave the loop together: the named barriers need all four warps
+        exact = bar_red_or(bar_id, 128, need || !ok);
+      }
+      if (exact) {
         if (bar_red_or(bar_id, 128, !ok)) {
           aborted = true;
           break;
         }
-        // exact maximum of this chunk for each row over the 128 tokens: the
-        // raw scaled scores (S^T(c) is still held) are transposed through scr
-        // and reduced per row
-        tmem_ld<kRS>(s_base + NR * (c & 1), x);
-        tc_wait_ld();
-        release_s();
+        // exact maximum of this chunk for each row over the 128 tokens: a
+        // reduce-scatter of d across the warp's lanes (lane l ends with row
+        // l % kRS), then across the four warps through shared memory
+        {
+          float v[kRS];
 #pragma unroll
-        for (int k = 0; k < kRS; ++k)
-          scr[tr_index(k, i)] = (masked && row0 + k < rmin) ? -CUDART_INF_F : __uint_as_float(x[k]) * cp.x;
+          for (int k = 0; k < kH; ++k) {
+            v[2 * k] = d[k].x;
+            v[2 * k + 1] = d[k].y;
+          }
+          warp_transpose_reduce<kRS, true>(v, lane);
+          if (lane < kRS) wmax[sw * 32 + lane] = v[0];
+        }
         named_bar(bar_id, 128);
-        if (rr < kRS) {
-          float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;
-#pragma unroll 1
-          for (int u = 0; u < 8; u += 2) {
-            const float4 a0 = *tr_seg(scr, rr, qt, u), a1 = *tr_seg(scr, rr, qt, u + 1);
-            m0 = fmax3(m0, fmaxf(a0.x, a0.y), fmaxf(a0.z, a0.w));
-            m1 = fmax3(m1, fmaxf(a1.x, a1.y), fmaxf(a1.z, a1.w));
+        if (i < kRS) {
+          const float cm = fmaxf(fmaxf(wmax[i], wmax[32 + i]), fmaxf(wmax[64 + i], wmax[96 + i]));
+          float shift = 0.f, al = 1.f;  // m_new = m_old + shift
+          if (cm > -CUDART_INF_F) {
+            if ((fr >> i) & 1u) {
+              shift = cm;  // first visible scores of this row: nothing to rescale
+              atomicAnd(fresh, ~(1u << i));
+            } else if (cm > 0.f) {
+              shift = cm;
+              al = ex2(-cm);
+            }
           }
-          float cm = fmaxf(m0, m1);
-          cm = fmaxf(cm, __shfl_xor_sync(kFull, cm, 1));
-          cm = fmaxf(cm, __shfl_xor_sync(kFull, cm, 2));
-          if (qt == 0) {
-            const float mo = -nms[rr], mn = fmaxf(mo, cm);
-            als[rr] = ex2(mo - mn);
-            nms[rr] = -mn;
-          }
+          als[i] = al;
+          dlt[i] = -shift;
+          nms[i] = nms[i] - shift;
         }
         named_bar(bar_id, 128);  // -m and the factors are complete
         bool change = false;
@@ -839,12 +899,12 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
           const float4* a4 = reinterpret_cast<const float4*>(als);
 #pragma unroll
           for (int q = 0; q < kRS / 4; ++q) {
-            const float4 a = a4[q];
-            l2[2 * q] = __fmul2_rn(l2[2 * q], make_float2(a.x, a.y));
-            z2[2 * q] = __fmul2_rn(z2[2 * q], make_float2(a.x, a.y));
-            l2[2 * q + 1] = __fmul2_rn(l2[2 * q + 1], make_float2(a.z, a.w));
-            z2[2 * q + 1] = __fmul2_rn(z2[2 * q + 1], make_float2(a.z, a.w));
-            change |= fminf(fminf(a.x, a.y), fminf(a.z, a.w)) < 1.0f;
+            const float4 al4 = a4[q];
+            l2[2 * q] = __fmul2_rn(l2[2 * q], make_float2(al4.x, al4.y));
+            z2[2 * q] = __fmul2_rn(z2[2 * q], make_float2(al4.x, al4.y));
+            l2[2 * q + 1] = __fmul2_rn(l2[2 * q + 1], make_float2(al4.z, al4.w));
+            z2[2 * q + 1] = __fmul2_rn(z2[2 * q + 1], make_float2(al4.z, al4.w));
+            change |= fminf(fminf(al4.x, al4.y), fminf(al4.z, al4.w)) < 1.0f;
           }
         }
         if (change && c > 0) {  // uniform across the warpgroup
@@ -865,10 +925,18 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
           }
           tc_wait_st();
         }
-        scores();
-        exps();
-      } else {
-        release_s();
+        // d and p again against the new maxima: d + m_old - m_new
+        {
+          const float4* t4 = reinterpret_cast<const float4*>(dlt);
+#pragma unroll
+          for (int q = 0; q < kRS / 4; ++q) {
+            const float4 tv = t4[q];
+            d[2 * q] = __fadd2_rn(d[2 * q], make_float2(tv.x, tv.y));
+            d[2 * q + 1] = __fadd2_rn(d[2 * q + 1], make_float2(tv.z, tv.w));
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kH; ++k) ph[k] = ex2_h2(d[k].x, d[k].y);
       }
       // row sums, zero term; P' = p * scale into the MN-major B tile
       uint32_t pk[kH];
@@ -908,27 +976,8 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     if (pre) tc_wait_ld();
     // ---- epilogue: l and the zero term of each row over all 128 tokens, by a
     // reduce-scatter across the warp's lanes (each step halves the rows a lane
-    // holds) and a sum of the four warps' partials in scr; then the output
-    // rows O^T / l staged in scr and stored
-    auto reduce_rows = [&](float(&v)[kRS]) -> float {  // lane's row: lane / (32 / kRS)
-#pragma unroll
-      for (int st = 0; st < 5; ++st) {
-        const int off = 16 >> st, n = kRS >> st;
-        if (n >= 2) {
-          const bool up = (lane & off) != 0;
-#pragma unroll
-          for (int k = 0; k < n / 2; ++k) {
-            const float send = up ? v[k] : v[k + n / 2];
-            const float keep = up ? v[k + n / 2] : v[k];
-            v[k] = keep + __shfl_xor_sync(kFull, send, off);
-          }
-        } else {
-          v[0] += __shfl_xor_sync(kFull, v[0], off);
-        }
-      }
-      return v[0];
-    };
-    named_bar(bar_id, 128);  // scr is free
+    // holds) and a sum of the four warps' partials; then the output rows
+    // O^T / l straight from tensor memory to global memory
     {
       constexpr int kLanesPerRow = 32 / kRS;
       float v[kRS];
@@ -937,25 +986,40 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         v[2 * k] = l2[k].x;
         v[2 * k + 1] = l2[k].y;
       }
-      const float lw = reduce_rows(v);
+      warp_transpose_reduce<kRS, false>(v, lane);
+      const float lw = v[0];
 #pragma unroll
       for (int k = 0; k < kH; ++k) {
         v[2 * k] = z2[k].x;
         v[2 * k + 1] = z2[k].y;
       }
-      const float zw = reduce_rows(v);
-      if (lane % kLanesPerRow == 0) {
-        scr[sw * 32 + lane / kLanesPerRow] = lw;
-        scr[128 + sw * 32 + lane / kLanesPerRow] = zw;
+      warp_transpose_reduce<kRS, false>(v, lane);
+      if (lane < kRS) {
+        (void)kLanesPerRow;
+        wsum[sw * 32 + lane] = lw;
+        wsum[128 + sw * 32 + lane] = v[0];
       }
     }
     named_bar(bar_id, 128);
-    float lrow = 0.f, zrow = 0.f;  // row i, in threads i < kRS
     if (i < kRS) {
+      float lrow = 0.f, zrow = 0.f;
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
-        lrow += scr[w * 32 + i];
-        zrow += scr[128 + w * 32 + i];
+        lrow += wsum[w * 32 + i];
+        zrow += wsum[128 + w * 32 + i];
+      }
+      const float inv = lrow > 0.f ? 1.0f / lrow : 0.f;
+      rcs[i] = make_float2(inv * 16777216.0f, zrow * inv);  // O^T holds codes as fp16 subnormals (code * 2^-24)
+      const int row = row0 + i;
+      if (row < a.R) {
+        const float lse = (aborted || *abort_flag) ? CUDART_NAN_F
+                                                   : (lrow > 0.f ? (-nms[i] + log2f(lrow)) * kLn2 : -CUDART_INF_F);
+        if constexpr (FUSED) {
+          a.part_lse[(((long)b * a.Hk + kvh) * a.S + split) * a.R + row] = lse;
+        } else {
+          const long orow = ((long)(row / a.group) * a.B + b) * a.Hq + kvh * a.group + row % a.group;
+          a.part_lse[orow * a.S + split] = lse;
+        }
       }
     }
     if (nchunks > 0) {
@@ -964,27 +1028,11 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       __syncwarp();
       tc_fence_after();
     }
+    named_bar(bar_id, 128);  // row constants ready
     aborted = aborted || (*abort_flag != 0u);
-    // the scratch partials of the single-launch verify are laid out
-    // [B][Hk][S][R][128] / [B][Hk][S][R] so that a CTA's rows are contiguous
-    const long fused_base = (((long)b * a.Hk + kvh) * a.S + split) * a.R;
-    if (i < kRS) {
-      const float inv = lrow > 0.f ? 1.0f / lrow : 0.f;
-      rcs[i] = make_float2(inv * 16777216.0f, zrow * inv);  // O^T holds codes as fp16 subnormals (code * 2^-24)
-      const int row = row0 + i;
-      if (row < a.R) {
-        const float lse = aborted ? CUDART_NAN_F : (lrow > 0.f ? (-nms[i] + log2f(lrow)) * kLn2 : -CUDART_INF_F);
-        if constexpr (FUSED) {
-          a.part_lse[fused_base + row] = lse;
-        } else {
-          const long orow = ((long)(row / a.group) * a.B + b) * a.Hq + kvh * a.group + row % a.group;
-          a.part_lse[orow * a.S + split] = lse;
-        }
-      }
-    }
-    named_bar(bar_id, 128);  // row constants ready, scr free
-    // output rows into scr[row][coordinate]: thread i holds coordinate i of O^T
     {
+      // thread i holds coordinate i of its rows: each row is 32 consecutive
+      // floats per warp, one 128-byte store
       uint32_t o[kRS];
       if (nchunks > 0) {
         tmem_ld<kRS>(tmem + lane_q + C::kTO + row0, o);
@@ -993,57 +1041,43 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
 #pragma unroll
         for (int k = 0; k < kRS; ++k) o[k] = 0u;
       }
+      if constexpr (FUSED) {
+        // the scratch partials of the single-launch verify are laid out
+        // [B][Hk][S][R][128] so that a CTA's rows are contiguous
+        float* dst = a.part_o + ((((long)b * a.Hk + kvh) * a.S + split) * a.R + row0) * kD + i;
 #pragma unroll
-      for (int k = 0; k < kRS; ++k) {
-        const float2 rc = rcs[k];
-        scr[k * 128 + i] = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rc.x, rc.y);
-      }
-    }
-    if constexpr (!FUSED) {
-      named_bar(bar_id, 128);
-      // warp sw stores rows sw, sw + 4, ... (512 contiguous bytes each); row
-      // r = n * group + jq is walked without divisions
-      int n = (row0 + sw) / a.group, jq = (row0 + sw) % a.group;
-      float4 v[kRS / 4];
-      long off[kRS / 4];
+        for (int k = 0; k < kRS; ++k) {
+          const float2 rc = rcs[k];
+          if (row0 + k < a.R) dst[k * kD] = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rc.x, rc.y);
+        }
+      } else {
+        int n = row0 / a.group, jq = row0 % a.group;
 #pragma unroll
-      for (int m = 0; m < kRS / 4; ++m) {
-        v[m] = reinterpret_cast<const float4*>(scr + (sw + 4 * m) * 128)[lane];
-        off[m] = ((((long)n * a.B + b) * a.Hq + kvh * a.group + jq) * a.S + split) * kD;
-        jq += 4;
-        while (jq >= a.group) {
-          jq -= a.group;
-          ++n;
+        for (int k = 0; k < kRS; ++k) {
+          const float2 rc = rcs[k];
+          if (row0 + k < a.R) {
+            const long orow = ((long)n * a.B + b) * a.Hq + kvh * a.group + jq;
+            a.part_o[(orow * a.S + split) * kD + i] = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rc.x, rc.y);
+          }
+          if (++jq == a.group) {
+            jq = 0;
+            ++n;
+          }
         }
       }
-#pragma unroll
-      for (int m = 0; m < kRS / 4; ++m)
-        if (row0 + sw + 4 * m < a.R) reinterpret_cast<float4*>(a.part_o + off[m])[lane] = v[m];
     }
     if constexpr (FUSED) {
       // ---- stage 2 in the same launch (a cooperative grid: every CTA is
-      // resident).  The warpgroup's rows leave scr as one bulk copy; once all
-      // S splits of this (sequence, kv-head) have written theirs, split s
-      // merges rows [s rpc, (s + 1) rpc).
-      named_bar(bar_id, 128);
-      // warp sw stores rows sw, sw + 4, ... (512 contiguous bytes each)
-#pragma unroll
-      for (int m = 0; m < kRS / 4; ++m) {
-        const int row = row0 + sw + 4 * m;
-        if (row < a.R)
-          __stcg(reinterpret_cast<float4*>(a.part_o + (fused_base + row) * kD) + lane,
-                 reinterpret_cast<const float4*>(scr + (sw + 4 * m) * 128)[lane]);
-      }
-      __threadfence();
+      // resident).  Once all S splits of this (sequence, kv-head) have
+      // written their rows, split s merges rows [s rpc, (s + 1) rpc).
       uint32_t* arrived = a.tickets + ((long)b * a.Hk + kvh) * 4;
       uint32_t* merged = arrived + 1;
       volatile uint32_t* go = reinterpret_cast<volatile uint32_t*>(sm + C::kMisc + 8);
       named_bar(15, 128 * C::kSW);  // this CTA's partial rows are written
       if (i == 0 && j == 0) {
-        __threadfence();  // ... and visible before the arrival counts
-        atomicAdd(arrived, 1u);
+        // one release covers the rows every thread of the CTA wrote before the barrier
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(arrived) : "memory");
         *go = spin_until_at_least(arrived, (uint32_t)a.S) ? 1u : 0u;
-        __threadfence();
       }
       named_bar(15, 128 * C::kSW);
       const bool failed = *go == 0u;
@@ -1097,6 +1131,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         // every split is past its wait: leave the counters zero for the next call
         atomicExch(arrived, 0u);
         atomicExch(merged, 0u);
+        atomicExch(arrived + 2, 0u);
       }
     }
   }
@@ -1146,7 +1181,8 @@ cudaError_t launch_tc(const VerifyArgs& a, cudaStream_t st) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const uint64_t bit = 1ull << dev;
   if (!(configured.load(std::memory_order_acquire) & bit)) {
     // setmaxnreg.inc waits for registers released by other warps of the CTA:
     // refuse to launch if the compiled register count cannot cover the split
@@ -1185,10 +1221,10 @@ cudaError_t launch_tc(const VerifyArgs& a, cudaStream_t st) {
 template <int PRESET, int NR>
 int fused_capacity() {
   using C = Cfg<PRESET, NR>;
-  static std::atomic<int> known[16];  // per device: 0 = not queried, else capacity + 1
+  static std::atomic<int> known[64];  // per device: 0 = not queried, else capacity + 1
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  int v = known[dev & 15].load(std::memory_order_acquire);
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  int v = known[dev].load(std::memory_order_acquire);
   if (v == 0) {
     auto kern = verify_stage1_tc_kernel<PRESET, NR, true>;
     int per_sm = 0, sms = 0;
@@ -1198,7 +1234,7 @@ int fused_capacity() {
       per_sm = sms = 0;
     cudaGetLastError();  // a refused query leaves no sticky error
     v = per_sm * sms + 1;
-    known[dev & 15].store(v, std::memory_order_release);
+    known[dev].store(v, std::memory_order_release);
   }
   return v - 1;
 }

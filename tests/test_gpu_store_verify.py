@@ -53,3 +53,51 @@ def test_store_verify_equals_store_then_verify(name, kw):
     torch.cuda.synchronize()
     assert torch.equal(sv.caches[1], sv.caches[0])
     assert torch.equal(sv.out, ref)
+
+
+# ---- tq_store_verify (the bench step) against the oracle itself: the cache
+# bytes after the call (prefix stored by tq_store, drafts by the call) and the
+# attention outputs, at the full workload sizes.
+
+@pytest.mark.parametrize("name", ["poc_k8v4", "poc_k3v4_nc", "decode_k3v4_nc"])
+def test_store_verify_matches_oracle(oracle_lib, name):
+    from quantized_kv_cache_store_gb300.step import SpecVerify
+    from tests.helpers import ATOL, assert_close, oracle_cache
+
+    inp = make_inputs(WORKLOADS[name], 1001)
+    sv = SpecVerify(inp)
+    sv.prefill()
+    sv.step_one(0)
+    torch.cuda.synchronize()
+    cache = oracle_cache(oracle_lib, inp)
+    assert np.array_equal(sv.caches[0].cpu().numpy(), cache)
+    wl = inp.wl
+    ref = oracle_lib.verify(wl.preset_id, cache, inp.q.numpy(), inp.block_table, inp.seq_lens, wl.causal)
+    assert assert_close(sv.out.cpu().numpy(), ref) < ATOL
+    assert not sv.tickets.any()
+
+
+def test_store_verify_longctx_sampled_rows(oracle_lib):
+    """Full-size long context through tq_store_verify: every page the drafts
+    touch is bit-exact against the oracle's encoding, and sampled output rows
+    match the oracle (each row needs the whole 262,144-token sequence)."""
+    from quantized_kv_cache_store_gb300.step import SpecVerify
+    from tests.helpers import assert_close
+
+    wl = WORKLOADS["longctx_k3v4_nc"]
+    inp = make_inputs(wl, 1001)
+    sv = SpecVerify(inp)
+    sv.prefill()
+    before = sv.caches[0].cpu().numpy()
+    sv.step_one(0)
+    torch.cuda.synchronize()
+    got = sv.caches[0].cpu().numpy()
+    # the oracle stores the drafts into the prefix-only cache the GPU started from
+    want = before.copy()
+    d = inp.draft_rows()
+    oracle_lib.store(wl.preset_id, want, inp.k.numpy()[d], inp.v.numpy()[d], inp.slots[d])
+    assert np.array_equal(got, want)
+    rows = [(0, 0, 0), (7, 0, 5), (3, 1, 31), (7, 1, 17), (1, 1, 8)]
+    ref = oracle_lib.verify(wl.preset_id, want, inp.q.numpy(), inp.block_table, inp.seq_lens, True, rows)
+    out = sv.out.cpu().numpy()
+    assert_close(np.stack([out[n, b, h] for n, b, h in rows]), ref)
