@@ -44,7 +44,9 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=1000)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="poc_k8v4", choices=list(CONFIG_INDEX))
-    p.add_argument("--also", default="poc_k3v4_nc", help="comma list of extra workloads ('' for none)")
+    p.add_argument("--also", default="poc_k3v4_nc,decode_k3v4_nc,longctx_k3v4_nc",
+                   help="comma list of extra workloads ('' for none)")
+    p.add_argument("--also-steps", type=int, default=400, help="timed steps of each extra workload (at most --steps)")
     p.add_argument("--splits", type=int, default=0, help="NUM_KV_SPLITS (0: the workload's)")
     p.add_argument("--graph-steps", type=int, default=500)
     p.add_argument("--e2e-steps", type=int, default=2000)
@@ -180,7 +182,7 @@ def ncu_traffic(kernel_tag: str, workload: str):
 
 # --------------------------------------------------------------- our arm
 
-def bench_workload(name, args, rank, world, pg, dev_props):
+def bench_workload(name, args, rank, world, pg, dev_props, steps=None):
     import torch
 
     from quantized_kv_cache_store_gb300 import tqkv
@@ -188,6 +190,7 @@ def bench_workload(name, args, rank, world, pg, dev_props):
     from quantized_kv_cache_store_gb300.step import SpecVerify
 
     wl = WORKLOADS[name]
+    steps = steps or args.steps
     S = args.splits or wl.num_kv_splits
     seed = 1000 + CONFIG_INDEX[name] + 100 * rank  # each rank is its own replica batch
     inp = make_inputs(wl, seed)
@@ -195,7 +198,7 @@ def bench_workload(name, args, rank, world, pg, dev_props):
     cache_bytes = inp.num_blocks * wl.Hk * page
     l2 = int(getattr(dev_props, "L2_cache_size", 128 << 20))
     n_caches = max(2, math.ceil(4 * l2 / cache_bytes))
-    G = max(1, min(args.graph_steps, args.steps))
+    G = max(1, min(args.graph_steps, steps))
     sv = SpecVerify(inp, num_kv_splits=S, n_caches=n_caches)
     sv.prefill()
     torch.cuda.synchronize()
@@ -216,7 +219,7 @@ def bench_workload(name, args, rank, world, pg, dev_props):
     torch.cuda.synchronize()
     step_graph = capture(G, 0, lambda i: sv.step_one(i))
     # K steps = full replays of G plus one shorter graph for the remainder
-    full, rem = divmod(args.steps, G)
+    full, rem = divmod(steps, G)
     rem_graph = capture(rem, 0, lambda i: sv.step_one(i)) if rem else None
     wfull, wrem = divmod(max(args.warmup, 3), G)
     wrem_graph = capture(wrem, 0, lambda i: sv.step_one(i)) if wrem else None
@@ -251,7 +254,17 @@ def bench_workload(name, args, rank, world, pg, dev_props):
     clocks.stop()
     clk = clocks.summary(t0, t1)
     elapsed_ms = max_over_ranks(pg, elapsed_ms)
-    us_per_step = elapsed_ms * 1e3 / args.steps
+    us_per_step = elapsed_ms * 1e3 / steps
+    # the same K-step region replayed a few more times: the spread of the value
+    spread = []
+    for _ in range(4):
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            run(full, rem_graph)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        spread.append(round(e0.elapsed_time(e1) * 1e3 / steps, 3))
 
     # per-kernel durations: each launch bracketed by external events in a graph
     kern_us = per_kernel_durations(sv, stream, G, n_caches)
@@ -267,7 +280,7 @@ def bench_workload(name, args, rank, world, pg, dev_props):
         vgraph.replay()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = max(1, min(20, args.steps // G))
+    reps = max(1, min(20, steps // G))
     with torch.cuda.stream(stream):
         ev0.record(stream)
         for _ in range(reps):
@@ -286,7 +299,7 @@ def bench_workload(name, args, rank, world, pg, dev_props):
                 "traffic": ncu_traffic("stage1", name), "algorithmic_bytes": alg_bytes,
                 "stage1_us": round(stage1_us, 3), "peak_source": peak_src}
     return dict(wl=wl, S=S, seed=seed, inp=inp, sv=sv, n_caches=n_caches, cache_bytes=cache_bytes,
-                us_per_step=us_per_step, verify_us=verify_us, kernels_us=kern_us, roofline=roof,
+                us_per_step=us_per_step, replays_us=spread, steps=steps, verify_us=verify_us, kernels_us=kern_us, roofline=roof,
                 clocks=clk, alg_bytes=alg_bytes, G=G, stream=stream)
 
 
@@ -429,7 +442,7 @@ def store_throughput(res, reps=5):
             "bytes": nbytes}
 
 
-def cpu_baseline(res, budget_s=12.0):
+def cpu_baseline(res, budget_s=12.0, max_calls=5):
     """The oracle as it stands (C, OpenMP over (sequence, kv-head)) on the
     host cores: store of the step's draft tokens + fp64 verify of every row,
     repeated while the budget lasts."""
@@ -447,7 +460,7 @@ def cpu_baseline(res, budget_s=12.0):
     q = inp.q.numpy()
     times = []
     t_start = time.time()
-    while not times or (time.time() - t_start < budget_s and len(times) < 5):
+    while not times or (time.time() - t_start < budget_s and len(times) < max_calls):
         t0 = time.perf_counter()
         oracle.store(wl.preset_id, cache, kd, vd, sd)
         oracle.verify(wl.preset_id, cache, q, inp.block_table, inp.seq_lens, wl.causal)
@@ -474,10 +487,16 @@ def run_ours(args):
     store_tp = store_throughput(main)
     also = {}
     for name in [x for x in args.also.split(",") if x and x != args.workload]:
-        r = bench_workload(name, args, rank, world, pg, props)
-        also[name] = {"us_per_step": round(r["us_per_step"] / world, 3), "verify_us": round(r["verify_us"], 3),
+        r = bench_workload(name, args, rank, world, pg, props, steps=min(args.steps, args.also_steps))
+        also[name] = {"us_per_step": round(r["us_per_step"] / world, 3), "steps": r["steps"],
+                      "replays_us": r["replays_us"], "verify_us": round(r["verify_us"], 3),
                       "kernels_us": _round(r["kernels_us"]), "roofline": r["roofline"],
-                      "num_kv_splits": r["S"], "clocks": r["clocks"]}
+                      "num_kv_splits": r["S"], "clocks": r["clocks"],
+                      "single_launch": single_launch(r["sv"])}
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            also[name]["cpu_baseline"] = cpu_baseline(r, budget_s=8.0, max_calls=2)
+        del r
+        torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(main)
@@ -497,6 +516,7 @@ def run_ours(args):
                    "l2": f"inputs larger than L2: {main['n_caches']} rotating cache copies of "
                          f"{main['cache_bytes'] / 1e6:.1f} MB",
                    "graph": f"CUDA graphs of {main['G']} steps"},
+        "replays_us": main["replays_us"],
         "verify_us": round(main["verify_us"], 3),
         "kernels_us": _round(main["kernels_us"]),
         "roofline": main["roofline"],

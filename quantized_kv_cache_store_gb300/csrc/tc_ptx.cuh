@@ -257,6 +257,14 @@ template <uint32_t R>
 __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(R));
 }
+// from the launch's per-thread register count L to R: an increase, a
+// decrease or nothing (setmaxnreg.dec may only lower, .inc only raise)
+template <int R, int L>
+__device__ __forceinline__ void regs_to() {
+  static_assert(R % 8 == 0 && R >= 24 && R <= 256, "setmaxnreg count");
+  if constexpr (R > L) regs_inc<R>();
+  else if constexpr (R < L) regs_dec<R>();
+}
 
 }  // namespace ptx
 }  // namespace tq

@@ -775,8 +775,9 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         poff[q] = lg ^ (((lg >> 7) & ((1u << C::kSwzBits) - 1u)) << 4);
       }
     }
-    // m starts at 0 for every row, marked fresh: a row's first visible
-    // scores take the exact path, which sets m to their maximum
+    // m starts at 0 for every row, marked fresh; on the first chunk, the
+    // rows that token 0 sees get m = its score + 4, and a fresh row's first
+    // visible scores elsewhere take the exact path
     if (i < kRS) nms[i] = 0.f;
     if (i == 0) *fresh = kRS == 32 ? 0xFFFFFFFFu : ((1u << kRS) - 1u);
     float2 l2[kH], z2[kH];  // l and the zero term of this token's rows (row pairs)
@@ -829,6 +830,36 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
           }
         }
       }
+      if (c == 0) {
+        // seed the running maxima from the chunk's first token (its scores,
+        // computed against m = 0, are raw): m = score + 4, so that the
+        // largest p of a row is rarely above 2^8 and rarely tiny
+        // (the seeds go through dlt: other threads may still be reading nms
+        // for their scores until the barrier)
+        if (i == 0) {
+          uint32_t seeded = 0;
+#pragma unroll
+          for (int k = 0; k < kH; ++k) {
+            const bool sx = d[k].x > -CUDART_INF_F, sy = d[k].y > -CUDART_INF_F;
+            dlt[2 * k] = sx ? -(d[k].x + 4.0f) : 0.f;
+            dlt[2 * k + 1] = sy ? -(d[k].y + 4.0f) : 0.f;
+            seeded |= (sx ? 1u : 0u) << (2 * k);
+            seeded |= (sy ? 1u : 0u) << (2 * k + 1);
+          }
+          *fresh = *fresh & ~seeded;
+        }
+        named_bar(bar_id, 128);
+        const float4* t4 = reinterpret_cast<const float4*>(dlt);
+#pragma unroll
+        for (int q = 0; q < kRS / 4; ++q) {
+          const float4 tv = t4[q];
+          d[2 * q] = __fadd2_rn(d[2 * q], make_float2(tv.x, tv.y));
+          d[2 * q + 1] = __fadd2_rn(d[2 * q + 1], make_float2(tv.z, tv.w));
+        }
+        // nms is next read after the vote below; dlt next written by the
+        // exact path after that vote
+        if (i < kRS) nms[i] = dlt[i];
+      }
       float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
 #pragma unroll
       for (int k = 0; k < kH; k += 2) {
@@ -837,27 +868,23 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       }
       // p = 2^d as fp16 pairs (the precision of the P' operand), issued
       // before the vote so that the vote's latency hides behind the
-      // exponentials; a vote for the exact path recomputes them.  The first
-      // chunk always takes the exact path (every row is fresh), without a vote.
+      // exponentials; a vote for the exact path recomputes them
       uint32_t ph[kH];
       const uint32_t fr = *fresh;
-      bool exact = c == 0;
-      if (c > 0) {
 #pragma unroll
-        for (int k = 0; k < kH; ++k) ph[k] = ex2_h2(d[k].x, d[k].y);
-        // exact path: some score above m + 8 (p could leave the fp16 range),
-        // or a row that has no maximum yet sees a score
-        bool need = fmaxf(mx0, mx1) > kRescaleThreshold;
-        if (fr != 0u) {
+      for (int k = 0; k < kH; ++k) ph[k] = ex2_h2(d[k].x, d[k].y);
+      // exact path: some score above m + 8 (p could leave the fp16 range),
+      // or a row that has no maximum yet sees a score
+      bool need = fmaxf(mx0, mx1) > kRescaleThreshold;
+      if (fr != 0u) {
 #pragma unroll
-          for (int k = 0; k < kH; ++k) {
-            need |= ((fr >> (2 * k)) & 1u) && d[k].x > -CUDART_INF_F;
-            need |= ((fr >> (2 * k + 1)) & 1u) && d[k].y > -CUDART_INF_F;
-          }
+        for (int k = 0; k < kH; ++k) {
+          need |= ((fr >> (2 * k)) & 1u) && d[k].x > -CUDART_INF_F;
+          need |= ((fr >> (2 * k + 1)) & 1u) && d[k].y > -CUDART_INF_F;
         }
-        // leave the loop together: the named barriers need all four warps
-        exact = bar_red_or(bar_id, 128, need || !ok);
       }
+      // leave the loop together: the named barriers need all four warps
+      const bool exact = bar_red_or(bar_id, 128, need || !ok);
       if (exact) {
         if (bar_red_or(bar_id, 128, !ok)) {
           aborted = true;
