@@ -73,6 +73,7 @@ struct VerifyArgs {
   int max_blocks;
   const int32_t* seq_lens;
   int n_spec, B, Hq, group, R, S, causal;
+  int rtiles;         // row tiles of up to 64 rows per (split, kv-head, sequence): ceil(R / 64)
   float* part_o;
   float* part_lse;
   float* out;         // merged output (single-launch verify only)
@@ -121,11 +122,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 cudaError_t launch_store(int preset, const StoreArgs& a, cudaStream_t st);
 cudaError_t launch_verify_stage1(int preset, const VerifyArgs& a, cudaStream_t st);
 cudaError_t launch_verify_stage2(const MergeArgs& a, cudaStream_t st);
-// tensor-core stage 1 (tcgen05), used for up to 64 query rows per kv-head
-bool verify_stage1_tc_supported(const VerifyArgs& a);
+// stage 1 on the tensor cores (tcgen05); rows beyond 64 per kv-head are
+// tiled across CTAs
 cudaError_t launch_verify_stage1_tc(int preset, const VerifyArgs& a, cudaStream_t st);
-// both stages in one cooperative launch (up to 64 rows per kv-head, S <= 32,
-// every CTA resident at once)
+// both stages in one cooperative launch (S <= 32, every CTA resident at once)
 bool verify_fused_supported(int preset, const VerifyArgs& a);
 cudaError_t launch_verify_fused(int preset, const VerifyArgs& a, cudaStream_t st);
 // sticky device-side error word (nonzero after a bounded wait expired)

@@ -108,8 +108,9 @@ tq_status verify_args(const tq_cache_desc* cache, const void* q, const int32_t* 
   if (causal != 0 && causal != 1) return TQ_ERR_INVALID_ARG;
   if (Hq % cache->num_kv_heads != 0) return TQ_ERR_INVALID_ARG;
   const int group = Hq / cache->num_kv_heads;
-  if (n_spec > 16 || n_spec * group > 128) return TQ_ERR_UNSUPPORTED;
-  if (num_kv_splits > 65535 || B > 65535 || max_blocks > (1 << 26)) return TQ_ERR_UNSUPPORTED;
+  if (n_spec > 128 || n_spec * group > 1024) return TQ_ERR_UNSUPPORTED;
+  const int rtiles = (n_spec * group + 63) / 64;
+  if (num_kv_splits > 65535 || (long)B * rtiles > 65535 || max_blocks > (1 << 26)) return TQ_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(partial_o, 16) ||
       !aligned(partial_lse, 4))
     return TQ_ERR_MISALIGNED;
@@ -126,6 +127,7 @@ tq_status verify_args(const tq_cache_desc* cache, const void* q, const int32_t* 
   a.Hq = Hq;
   a.group = group;
   a.R = n_spec * group;
+  a.rtiles = rtiles;
   a.S = num_kv_splits;
   a.causal = causal;
   a.part_o = partial_o;

@@ -288,7 +288,12 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
   const Bars bars{sbase + C::kBar, C::kStages};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  // rows beyond 64 per kv-head are tiled across CTAs: this CTA takes rows
+  // [row_off, row_off + Rt) of its (split, kv-head, sequence); the tiles of
+  // a split stream the same pages (L2 serves the repeats)
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z / a.rtiles, rt = blockIdx.z % a.rtiles;
+  const int row_off = rt * NR, Rt = min(a.R - row_off, NR);
+  const int unit = rt * a.S + split;  // this CTA among the S x rtiles of its pair
   pdl_wait();
   pdl_trigger();
 
@@ -405,8 +410,8 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       float x[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) x[e] = 0.f;
-      if (r < a.R) {
-        const int n = r / a.group, jq = r % a.group;
+      if (r < Rt) {
+        const int n = (row_off + r) / a.group, jq = (row_off + r) % a.group;
         const uint4* qp = reinterpret_cast<const uint4*>(
             a.q + (((long)n * a.B + b) * a.Hq + kvh * a.group + jq) * kD + 16 * part);
 #pragma unroll
@@ -483,7 +488,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
           // chunk prefill wait for a free ring stage anyway); skipped drafts
           // (no position, invalid block) count too
           uint32_t count = 0;
-          for (int n = split; n < a.n_spec; n += a.S) {
+          for (int n = unit; n < a.n_spec; n += a.S * a.rtiles) {
             ++count;
             const int pos = L_b - a.n_spec + n;
             if (pos < 0) continue;
@@ -689,7 +694,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
           rmin = 0;
           if (a.causal) {
             const int nmin = pos - L_b + a.n_spec;  // draft n sees this token iff n >= nmin
-            rmin = nmin <= 0 ? 0 : nmin * a.group;
+            rmin = nmin <= 0 ? 0 : max(0, nmin * a.group - row_off);  // first visible row of the tile
           }
         }
         colp[(c & 3) * 128 + i] = make_float4(cs, sv, zv, __int_as_float(rmin));
@@ -775,9 +780,8 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         poff[q] = lg ^ (((lg >> 7) & ((1u << C::kSwzBits) - 1u)) << 4);
       }
     }
-    // m starts at 0 for every row, marked fresh; on the first chunk, the
-    // rows that token 0 sees get m = its score + 4, and a fresh row's first
-    // visible scores elsewhere take the exact path
+    // m starts at 0 for every row, marked fresh: a row's first visible
+    // scores take the exact path, which sets m to their maximum
     if (i < kRS) nms[i] = 0.f;
     if (i == 0) *fresh = kRS == 32 ? 0xFFFFFFFFu : ((1u << kRS) - 1u);
     float2 l2[kH], z2[kH];  // l and the zero term of this token's rows (row pairs)
@@ -830,36 +834,6 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
           }
         }
       }
-      if (c == 0) {
-        // seed the running maxima from the chunk's first token (its scores,
-        // computed against m = 0, are raw): m = score + 4, so that the
-        // largest p of a row is rarely above 2^8 and rarely tiny
-        // (the seeds go through dlt: other threads may still be reading nms
-        // for their scores until the barrier)
-        if (i == 0) {
-          uint32_t seeded = 0;
-#pragma unroll
-          for (int k = 0; k < kH; ++k) {
-            const bool sx = d[k].x > -CUDART_INF_F, sy = d[k].y > -CUDART_INF_F;
-            dlt[2 * k] = sx ? -(d[k].x + 4.0f) : 0.f;
-            dlt[2 * k + 1] = sy ? -(d[k].y + 4.0f) : 0.f;
-            seeded |= (sx ? 1u : 0u) << (2 * k);
-            seeded |= (sy ? 1u : 0u) << (2 * k + 1);
-          }
-          *fresh = *fresh & ~seeded;
-        }
-        named_bar(bar_id, 128);
-        const float4* t4 = reinterpret_cast<const float4*>(dlt);
-#pragma unroll
-        for (int q = 0; q < kRS / 4; ++q) {
-          const float4 tv = t4[q];
-          d[2 * q] = __fadd2_rn(d[2 * q], make_float2(tv.x, tv.y));
-          d[2 * q + 1] = __fadd2_rn(d[2 * q + 1], make_float2(tv.z, tv.w));
-        }
-        // nms is next read after the vote below; dlt next written by the
-        // exact path after that vote
-        if (i < kRS) nms[i] = dlt[i];
-      }
       float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
 #pragma unroll
       for (int k = 0; k < kH; k += 2) {
@@ -868,23 +842,28 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       }
       // p = 2^d as fp16 pairs (the precision of the P' operand), issued
       // before the vote so that the vote's latency hides behind the
-      // exponentials; a vote for the exact path recomputes them
+      // exponentials; a vote for the exact path recomputes them.  The first
+      // chunk always takes the exact path (every row is fresh), without a
+      // vote: each row's largest p is then exactly 1.
       uint32_t ph[kH];
       const uint32_t fr = *fresh;
+      bool exact = c == 0;
+      if (c > 0) {
 #pragma unroll
-      for (int k = 0; k < kH; ++k) ph[k] = ex2_h2(d[k].x, d[k].y);
-      // exact path: some score above m + 8 (p could leave the fp16 range),
-      // or a row that has no maximum yet sees a score
-      bool need = fmaxf(mx0, mx1) > kRescaleThreshold;
-      if (fr != 0u) {
+        for (int k = 0; k < kH; ++k) ph[k] = ex2_h2(d[k].x, d[k].y);
+        // exact path: some score above m + 8 (p could leave the fp16 range),
+        // or a row that has no maximum yet sees a score
+        bool need = fmaxf(mx0, mx1) > kRescaleThreshold;
+        if (fr != 0u) {
 #pragma unroll
-        for (int k = 0; k < kH; ++k) {
-          need |= ((fr >> (2 * k)) & 1u) && d[k].x > -CUDART_INF_F;
-          need |= ((fr >> (2 * k + 1)) & 1u) && d[k].y > -CUDART_INF_F;
+          for (int k = 0; k < kH; ++k) {
+            need |= ((fr >> (2 * k)) & 1u) && d[k].x > -CUDART_INF_F;
+            need |= ((fr >> (2 * k + 1)) & 1u) && d[k].y > -CUDART_INF_F;
+          }
         }
+        // leave the loop together: the named barriers need all four warps
+        exact = bar_red_or(bar_id, 128, need || !ok);
       }
-      // leave the loop together: the named barriers need all four warps
-      const bool exact = bar_red_or(bar_id, 128, need || !ok);
       if (exact) {
         if (bar_red_or(bar_id, 128, !ok)) {
           aborted = true;
@@ -1037,8 +1016,8 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       }
       const float inv = lrow > 0.f ? 1.0f / lrow : 0.f;
       rcs[i] = make_float2(inv * 16777216.0f, zrow * inv);  // O^T holds codes as fp16 subnormals (code * 2^-24)
-      const int row = row0 + i;
-      if (row < a.R) {
+      const int row = row_off + row0 + i;  // row of the kv-head's R
+      if (row0 + i < Rt) {
         const float lse = (aborted || *abort_flag) ? CUDART_NAN_F
                                                    : (lrow > 0.f ? (-nms[i] + log2f(lrow)) * kLn2 : -CUDART_INF_F);
         if constexpr (FUSED) {
@@ -1071,18 +1050,18 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       if constexpr (FUSED) {
         // the scratch partials of the single-launch verify are laid out
         // [B][Hk][S][R][128] so that a CTA's rows are contiguous
-        float* dst = a.part_o + ((((long)b * a.Hk + kvh) * a.S + split) * a.R + row0) * kD + i;
+        float* dst = a.part_o + ((((long)b * a.Hk + kvh) * a.S + split) * a.R + row_off + row0) * kD + i;
 #pragma unroll
         for (int k = 0; k < kRS; ++k) {
           const float2 rc = rcs[k];
-          if (row0 + k < a.R) dst[k * kD] = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rc.x, rc.y);
+          if (row0 + k < Rt) dst[k * kD] = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rc.x, rc.y);
         }
       } else {
-        int n = row0 / a.group, jq = row0 % a.group;
+        int n = (row_off + row0) / a.group, jq = (row_off + row0) % a.group;
 #pragma unroll
         for (int k = 0; k < kRS; ++k) {
           const float2 rc = rcs[k];
-          if (row0 + k < a.R) {
+          if (row0 + k < Rt) {
             const long orow = ((long)n * a.B + b) * a.Hq + kvh * a.group + jq;
             a.part_o[(orow * a.S + split) * kD + i] = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rc.x, rc.y);
           }
@@ -1104,11 +1083,12 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       if (i == 0 && j == 0) {
         // one release covers the rows every thread of the CTA wrote before the barrier
         asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(arrived) : "memory");
-        *go = spin_until_at_least(arrived, (uint32_t)a.S) ? 1u : 0u;
+        *go = spin_until_at_least(arrived, (uint32_t)(a.S * a.rtiles)) ? 1u : 0u;
       }
       named_bar(15, 128 * C::kSW);
       const bool failed = *go == 0u;
-      const int rpc = (a.R + a.S - 1) / a.S, r_lo = split * rpc, r_hi = min(a.R, r_lo + rpc);
+      const int nu = a.S * a.rtiles;
+      const int rpc = (a.R + nu - 1) / nu, r_lo = unit * rpc, r_hi = min(a.R, r_lo + rpc);
       const int w8 = warp - 8;
       constexpr int kMW = 4 * C::kSW;  // merging warps, a warp per row, lane l: coordinates 4l .. 4l+3
       const long pair_base = ((long)b * a.Hk + kvh) * a.S * a.R;  // split 0, row 0 of this (sequence, kv-head)
@@ -1154,7 +1134,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         reinterpret_cast<float4*>(a.out + orow * kD)[lane] = acc;
       }
       named_bar(15, 128 * C::kSW);
-      if (i == 0 && j == 0 && atomicAdd(merged, 1u) == (uint32_t)a.S - 1u) {
+      if (i == 0 && j == 0 && atomicAdd(merged, 1u) == (uint32_t)(a.S * a.rtiles) - 1u) {
         // every split is past its wait: leave the counters zero for the next call
         atomicExch(arrived, 0u);
         atomicExch(merged, 0u);
@@ -1228,7 +1208,7 @@ cudaError_t launch_tc(const VerifyArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.S, a.Hk, a.B);
+  cfg.gridDim = dim3(a.S, a.Hk, a.B * a.rtiles);
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = st;
@@ -1268,7 +1248,6 @@ int fused_capacity() {
 
 }  // namespace
 
-bool verify_stage1_tc_supported(const VerifyArgs& a) { return a.R <= 64; }
 
 cudaError_t launch_verify_stage1_tc(int preset, const VerifyArgs& a, cudaStream_t st) {
   if (preset == 0) {
@@ -1282,9 +1261,9 @@ cudaError_t launch_verify_stage1_tc(int preset, const VerifyArgs& a, cudaStream_
 }
 
 bool verify_fused_supported(int preset, const VerifyArgs& a) {
-  if (a.R > 64 || a.S > 32) return false;
+  if (a.S > 32) return false;
   // every CTA resident at once (the merge waits for all splits)
-  const long ctas = (long)a.S * a.Hk * a.B;
+  const long ctas = (long)a.S * a.Hk * a.B * a.rtiles;
   int cap = 0;
   if (preset == 0) cap = a.R <= 16 ? fused_capacity<0, 16>() : a.R <= 32 ? fused_capacity<0, 32>() : fused_capacity<0, 64>();
   else cap = a.R <= 16 ? fused_capacity<1, 16>() : a.R <= 32 ? fused_capacity<1, 32>() : fused_capacity<1, 64>();

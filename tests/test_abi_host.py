@@ -92,9 +92,9 @@ def test_stage1_validation(lib):
     assert _s1(lib, None) == tqkv.TQ_ERR_INVALID_ARG
     assert _s1(lib, d, q=0) == tqkv.TQ_ERR_INVALID_ARG
     assert _s1(lib, d, n=0) == tqkv.TQ_ERR_INVALID_ARG
-    assert _s1(lib, d, n=17) == tqkv.TQ_ERR_UNSUPPORTED
+    assert _s1(lib, d, n=129) == tqkv.TQ_ERR_UNSUPPORTED     # more than 128 query tokens per sequence
     assert _s1(lib, d, Hq=30) == tqkv.TQ_ERR_INVALID_ARG       # Hq % Hk != 0
-    assert _s1(lib, d, Hq=128) == tqkv.TQ_ERR_UNSUPPORTED      # 8 drafts x 32 heads per kv-head > 128 rows
+    assert _s1(lib, d, n=64, Hq=128) == tqkv.TQ_ERR_UNSUPPORTED  # 64 x 32 rows per kv-head > 1024
     assert _s1(lib, d, S=0) == tqkv.TQ_ERR_INVALID_ARG
     assert _s1(lib, d, S=70000) == tqkv.TQ_ERR_UNSUPPORTED
     assert _s1(lib, d, causal=2) == tqkv.TQ_ERR_INVALID_ARG

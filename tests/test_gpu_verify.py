@@ -304,3 +304,32 @@ def test_single_call_verify_poc(oracle_lib, name):
     assert_close(fused, _oracle_out(oracle_lib, inp))
     assert_close(fused, staged, atol=1e-5, rtol=1e-5, what="single call vs two calls")
     assert tqkv.tq_device_status() == tqkv.TQ_OK
+
+
+# ---- continuation chunks ("spec-decode-intel-arc", backend-integration
+# section: chunks of up to 128 query tokens take the spec-verify path): up to
+# 1024 query rows per kv-head, tiled 64 rows per CTA on the tensor cores.
+
+@pytest.mark.parametrize("preset", ["k8v4", "k3v4_nc"])
+@pytest.mark.parametrize("q_len,group,L,S", [(16, 8, 300, 3), (64, 4, 700, 2), (128, 8, 600, 2), (128, 2, 1500, 5)])
+def test_continuation_chunks_match_oracle(oracle_lib, preset, q_len, group, L, S):
+    from quantized_kv_cache_store_gb300.step import SpecVerify
+
+    wl = _wl(preset, q_len, 2, 2 * group, 2, L, S, True)
+    inp = make_inputs(wl, 31)
+    ref = _oracle_out(oracle_lib, inp)
+    # stage 1 + stage 2
+    cache, po, pl, out = gpu_run(inp)
+    assert np.array_equal(cache, oracle_cache(oracle_lib, inp))
+    assert_close(out, ref)
+    # one tq_verify call and one tq_store_verify call
+    sv = SpecVerify(inp, n_caches=2)
+    sv.prefill()
+    sv.store(0)
+    fused = sv.verify_call(0).cpu().numpy()
+    assert_close(fused, ref)
+    sv.step_one(1)
+    torch.cuda.synchronize()
+    assert torch.equal(sv.caches[1], sv.caches[0])
+    assert_close(sv.out.cpu().numpy(), ref)
+    assert not sv.tickets.any()
