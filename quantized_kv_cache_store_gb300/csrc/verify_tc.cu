@@ -35,8 +35,8 @@
 // bounded by 2^8 and the stale maximum is used (any reference point gives the
 // same softmax).
 //
-// Warp roles: warp 0 = producer (block ids + copies), warp 1 = MMA issuer,
-// warp 2 = TMEM owner; warpgroup 1 dequantises chunk c (A_K[c % 2], A_V[c % 3]
+// Warp roles: warps 0, 2, 3 = producers (block ids + copies), warp 1 = MMA
+// issuer and TMEM owner; warpgroup 1 dequantises chunk c (A_K[c % 2], A_V[c % 3]
 // and the per-token parameters) while softmax warpgroup j (rows [32 j,
 // 32 j + 32)) works on an earlier chunk.  Every wait on an mbarrier is
 // bounded: on expiry the CTA sets an abort flag and the sticky device error
@@ -297,6 +297,22 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
   pdl_wait();
   pdl_trigger();
 
+  // ---- this thread's part of the query rows, requested before anything else
+  // (it depends on nothing but the launch): set-up thread t = tid - 128 < 4 NR
+  // takes row r = t / 4, coordinates [32 (t % 4), 32 (t % 4) + 32)
+  const int q_item = tid - 128, q_r = q_item >> 2, q_part = q_item & 3;
+  const bool q_mine = tid >= 128 && q_item < 4 * NR;
+  uint4 qv[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) qv[u] = make_uint4(0u, 0u, 0u, 0u);
+  if (q_mine && q_r < Rt) {
+    const int n = (row_off + q_r) / a.group, jq = (row_off + q_r) % a.group;
+    const uint4* qp =
+        reinterpret_cast<const uint4*>(a.q + (((long)n * a.B + b) * a.Hq + kvh * a.group + jq) * kD + 32 * q_part);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) qv[u] = qp[u];
+  }
+
   // ---- this split's token range
   int L_b = a.seq_lens[b];
   L_b = max(0, min(L_b, a.max_blocks * kBlock));
@@ -367,8 +383,8 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     ids_next = fetch_ids(4);
   }
 
-  // ---- set-up: barriers, tensor memory
-  if (tid == 0) {
+  // ---- set-up: barriers, tensor memory (warp 1, which loads no block ids)
+  if (tid == 32) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bars.full(s), C::kProducers);
       mbar_init(bars.empty(s), 4);
@@ -386,95 +402,90 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == 2) {
+  if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
-  cta_bar();  // barriers initialised
+  tc_fence_before();
+  cta_bar();  // barriers initialised, tensor memory allocated
+  tc_fence_after();
 
   // the whole ring goes out at once (up to the chunk holding drafts this
   // split stores first); the first chunk lands about as early as when it
-  // is requested alone
+  // is requested alone.  The producers go on to their loop without waiting
+  // for the rest of the set-up.
   const int prefill = min(min(nchunks, C::kStages), min(c_draft, 4));
   if (producer)
     for (int c = 0; c < prefill; ++c) produce(c);
 
-  // ---- query rows (dequant + softmax warpgroups) and code-pair table (warps 2-3)
+  // ---- query rows and code-pair table (dequant + softmax warpgroups); the
+  // other warps that need them (MMA issuer) wait on named barrier 14
   if (tid >= 128) {
     // Q rows r = n * group + jq (zero beyond R) into the K-major, 128B-swizzled
     // B operand: row r, coordinate d at block d/64, line r, 16-byte chunk
-    // ((d % 64) / 8) ^ (r % 8).  Eight threads per row, 16 coordinates each;
-    // k3v4_nc rotates the rows: q_rot = H q / sqrt(128).
-    for (int item = tid - 128; item < NR * 8; item += C::kThreads - 128) {
-      const int r = item >> 3, part = item & 7;
-      float x[16];
+    // ((d % 64) / 8) ^ (r % 8).  k3v4_nc rotates the rows:
+    // q_rot = H diag(signs) q / sqrt(128).
+    if (q_mine) {
+      float x[32];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) x[e] = 0.f;
-      if (r < Rt) {
-        const int n = (row_off + r) / a.group, jq = (row_off + r) % a.group;
-        const uint4* qp = reinterpret_cast<const uint4*>(
-            a.q + (((long)n * a.B + b) * a.Hq + kvh * a.group + jq) * kD + 16 * part);
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t w[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const uint4 v4 = qp[u];
-          const uint32_t w[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __half2 h2 = *reinterpret_cast<const __half2*>(&w[e]);
-            x[8 * u + 2 * e] = __low2float(h2);
-            x[8 * u + 2 * e + 1] = __high2float(h2);
-          }
+        for (int e = 0; e < 4; ++e) {
+          const __half2 h2 = *reinterpret_cast<const __half2*>(&w[e]);
+          x[8 * u + 2 * e] = __low2float(h2);
+          x[8 * u + 2 * e + 1] = __high2float(h2);
         }
       }
       if (PRESET == 1) {
-        // k3v4_nc_rs: q_rot = H diag(s) q / sqrt(128), signs of coordinates 16 part + e
-        const uint32_t sg = (a.signs[part >> 1] >> (16 * (part & 1))) & 0xFFFFu;
+        // signs of coordinates 32 part + e, then the butterflies of strides
+        // 1 .. 16 in the thread and 32, 64 across the row's four threads
+        const uint32_t sg = a.signs[q_part];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
+        for (int e = 0; e < 32; ++e)
           if ((sg >> e) & 1u) x[e] = -x[e];
-      }
-      if (PRESET == 1) {
 #pragma unroll
-        for (int hs = 1; hs < 16; hs <<= 1)
+        for (int hs = 1; hs < 32; hs <<= 1)
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
+          for (int e = 0; e < 32; ++e)
             if (!(e & hs)) {
               const float u = x[e], v = x[e + hs];
               x[e] = u + v;
               x[e + hs] = u - v;
             }
 #pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {  // strides 16, 32, 64: partner thread part ^ o
-          const bool upper = (part & o) != 0;
+        for (int o = 1; o < 4; o <<= 1) {  // partner thread part ^ o
+          const bool upper = (q_part & o) != 0;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
+          for (int e = 0; e < 32; ++e) {
             const float pv = __shfl_xor_sync(kFull, x[e], o);
             x[e] = upper ? pv - x[e] : x[e] + pv;
           }
         }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) x[e] *= 0.08838834764831845f;
+        for (int e = 0; e < 32; ++e) x[e] *= 0.08838834764831845f;
       }
 #pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        const int d0 = 16 * part + 8 * hc;  // first coordinate of this 16-byte chunk
-        uint8_t* rowp = sm + C::kQ + (d0 >> 6) * (NR * 128) + (r >> 3) * 1024 + (r & 7) * 128;
+      for (int hc = 0; hc < 4; ++hc) {
+        const int d0 = 32 * q_part + 8 * hc;  // first coordinate of this 16-byte chunk
+        uint8_t* rowp = sm + C::kQ + (d0 >> 6) * (NR * 128) + (q_r >> 3) * 1024 + (q_r & 7) * 128;
         const int chunk16 = (d0 & 63) >> 3;
-        *reinterpret_cast<uint4*>(rowp + ((chunk16 ^ (r & 7)) << 4)) =
+        *reinterpret_cast<uint4*>(rowp + ((chunk16 ^ (q_r & 7)) << 4)) =
             make_uint4(pack_half2(x[8 * hc + 0], x[8 * hc + 1]), pack_half2(x[8 * hc + 2], x[8 * hc + 3]),
                        pack_half2(x[8 * hc + 4], x[8 * hc + 5]), pack_half2(x[8 * hc + 6], x[8 * hc + 7]));
       }
     }
-  } else if (PRESET == 1 && tid >= 64) {
-    for (int i = tid - 64; i < 64 * 32; i += 64) {
-      const int e = i >> 5;
-      pairs[i] = (uint32_t)a.cb.c[e & 7] | ((uint32_t)a.cb.c[e >> 3] << 16);
+    if (PRESET == 1) {
+      for (int i = tid - 128; i < 64 * 32; i += C::kThreads - 128) {
+        const int e = i >> 5;
+        pairs[i] = (uint32_t)a.cb.c[e & 7] | ((uint32_t)a.cb.c[e >> 3] << 16);
+      }
     }
   }
-  fence_async_smem();
-  tc_fence_before();
-  cta_bar();
-  tc_fence_after();
+  if (!producer) {
+    fence_async_smem();
+    named_bar(14, C::kThreads - 32 * C::kProducers);
+  }
   const uint32_t tmem = *tmem_slot;
   const float sl2 = kLog2e * 0.08838834764831845f;  // log2(e) / sqrt(128)
 
@@ -595,7 +606,8 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
                 break;
               }
             }
-            __nanosleep(20);
+            // no sleep between polls: a sleep's granularity (hundreds of
+            // cycles) would delay every MMA by as much
           } else {
             idle = 0;
             idle_since = 0;
@@ -1146,7 +1158,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
   // ---- teardown: every role has drained its asynchronous work
   tc_fence_before();
   cta_bar();
-  if (warp == 2) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
