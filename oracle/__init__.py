@@ -67,6 +67,19 @@ def _load():
             lib.oracle_lloyd_max8.argtypes = [P]
             lib.oracle_codebook16.restype = I
             lib.oracle_codebook16.argtypes = [P]
+            lib.oracle_lloyd_max.restype = I
+            lib.oracle_lloyd_max.argtypes = [I, P]
+            lib.oracle_codebook_n.restype = I
+            lib.oracle_codebook_n.argtypes = [I, P]
+            lib.oracle_key_bits.restype = I
+            lib.oracle_key_bits.argtypes = [I]
+            lib.oracle_key_levels.restype = I
+            lib.oracle_key_levels.argtypes = [I]
+            lib.oracle_quant_index_n.restype = I
+            lib.oracle_quant_index_n.argtypes = [ctypes.c_float, P, I]
+            lib.oracle_pack_bits.argtypes = [P, I, P]
+            lib.oracle_unpack_bits.argtypes = [P, I, P]
+            lib.oracle_encode_keyq.argtypes = [P, P, I, P, P, I, I]
             lib.oracle_wht_f32.argtypes = [P]
             lib.oracle_wht_f64.argtypes = [P]
             lib.oracle_tree_sum.restype = ctypes.c_float
@@ -152,6 +165,33 @@ def codebook16() -> np.ndarray:
     return cb
 
 
+def lloyd_max(n: int) -> tuple[np.ndarray, int]:
+    """n-level Lloyd-Max levels of the standard normal (fp64) and the iteration count."""
+    c = np.zeros(n, np.float64)
+    it = _load().oracle_lloyd_max(n, _ptr(c))
+    return c, int(it)
+
+
+def codebook_n(n: int) -> np.ndarray:
+    """n-level key codebook for N(0, 1/128), fp16 bit patterns, ascending."""
+    cb = np.zeros(n, np.uint16)
+    _load().oracle_codebook_n(n, _ptr(cb))
+    return cb
+
+
+def key_bits(preset: int) -> int:
+    return int(_load().oracle_key_bits(preset))
+
+
+def key_levels(preset: int) -> int:
+    return int(_load().oracle_key_levels(preset))
+
+
+def codebook(preset: int) -> np.ndarray:
+    """The key codebook of a coded-key preset (fp16 bit patterns)."""
+    return codebook_n(key_levels(preset))
+
+
 def wht_f32(x) -> np.ndarray:
     t = np.ascontiguousarray(x, dtype=np.float32).copy()
     _load().oracle_wht_f32(_ptr(t))
@@ -172,6 +212,35 @@ def tree_sum(a) -> float:
 def quant_index(y: float, cb: np.ndarray | None = None) -> int:
     cb = codebook16() if cb is None else _u16(cb)
     return int(_load().oracle_quant_index(ctypes.c_float(y), _ptr(cb)))
+
+
+def quant_index_n(y: float, cb) -> int:
+    cb = _u16(cb)
+    return int(_load().oracle_quant_index_n(ctypes.c_float(y), _ptr(cb), len(cb)))
+
+
+def pack_bits(idx, bits: int) -> np.ndarray:
+    idx = np.ascontiguousarray(idx, dtype=np.uint8)
+    out = np.zeros(HEAD_DIM * bits // 8, np.uint8)
+    _load().oracle_pack_bits(_ptr(idx), bits, _ptr(out))
+    return out
+
+
+def unpack_bits(b, bits: int) -> np.ndarray:
+    b = np.ascontiguousarray(b, dtype=np.uint8)
+    out = np.zeros(HEAD_DIM, np.uint8)
+    _load().oracle_unpack_bits(_ptr(b), bits, _ptr(out))
+    return out
+
+
+def encode_keyq(k, bits: int, corrected: bool = True) -> tuple[np.ndarray, int]:
+    """Coded key with a 2^bits-level codebook: (code bytes, fp16 key factor bits)."""
+    k = _u16(k)
+    cb = codebook_n(1 << bits)
+    codes = np.zeros(HEAD_DIM * bits // 8, np.uint8)
+    nc = np.zeros(1, np.uint16)
+    _load().oracle_encode_keyq(_ptr(k), _ptr(cb), bits, _ptr(codes), _ptr(nc), int(corrected), 0)
+    return codes, int(nc[0])
 
 
 def pack3(idx) -> np.ndarray:
@@ -226,7 +295,7 @@ def encode_value4(v) -> tuple[np.ndarray, int, int]:
 
 def decode_key(preset: int, page: np.ndarray, off: int) -> np.ndarray:
     page = np.ascontiguousarray(page, dtype=np.uint8)
-    cb = codebook16()
+    cb = codebook(preset) if key_bits(preset) else codebook16()
     out = np.zeros(HEAD_DIM, np.float64)
     _load().oracle_decode_key(preset, _ptr(page), off, _ptr(cb), _ptr(out))
     return out

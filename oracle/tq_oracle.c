@@ -23,8 +23,9 @@
  *         log-sum-exp reduction).
  *
  * Readings where the pages are silent (the GPU library follows the same ones):
- *   - codebook: 8-level Lloyd-Max for N(0, 1/D), derived in fp64 and rounded
- *     to fp16; decision boundaries are fp32 midpoints of adjacent centroids;
+ *   - codebook: 8-level (k3 presets), 16-level (k4v4_nc) or 4-level (k2v4_nc)
+ *     Lloyd-Max for N(0, 1/D), derived in fp64 and rounded to fp16; decision
+ *     boundaries are fp32 midpoints of adjacent centroids;
  *   - rotation: unnormalised Sylvester Walsh-Hadamard butterflies (h = 1, 2,
  *     4, ..., 64), no random signs; the rotated unit vector is H k / (|k| sqrt D);
  *   - norm correction: nc = |k| / |c_hat| stored as fp16;
@@ -32,7 +33,7 @@
  *     up to fp16, codes rounded half-to-even and clamped to [0, 15];
  *   - FP8 keys: e4m3, round-to-nearest-even, saturating to +-448, NaN -> 0x7F,
  *     no scale and no rotation;
- *   - bit order: 3-bit codes LSB-first in a little-endian stream; value codes
+ *   - bit order: key codes LSB-first in a little-endian stream; value codes
  *     coordinate-major (byte 8d + t/2, low nibble = even token t); the page for
  *     one (block, kv-head) is planar (below).
  *
@@ -48,13 +49,28 @@
 #define D 128
 #define BLK 16
 
-enum { PRESET_K8V4 = 0, PRESET_K3V4_NC = 1, PRESET_K3V4 = 2, PRESET_K3V4_NC_RS = 3 };
+enum {
+  PRESET_K8V4 = 0,
+  PRESET_K3V4_NC = 1,
+  PRESET_K3V4 = 2,
+  PRESET_K3V4_NC_RS = 3,
+  PRESET_K4V4_NC = 4,
+  PRESET_K2V4_NC = 5
+};
 /* k3v4_nc, k3v4 and k3v4_nc_rs share the key coding and the page; k3v4
  * stores the plain norm |k| as the key factor instead of the corrected
  * |k| / |c_hat|; k3v4_nc_rs rotates by H diag(s) instead of H, s a fixed
- * random sign vector */
+ * random sign vector.  k4v4_nc and k2v4_nc are k3v4_nc with 16- and 4-level
+ * codebooks (the other widths of "3-4 bit" TurboQuant, [SD] "Context"). */
 static int is_k3(int preset) {
   return preset == PRESET_K3V4_NC || preset == PRESET_K3V4 || preset == PRESET_K3V4_NC_RS;
+}
+/* bits per key code: 0 for the FP8 keys of k8v4 */
+int oracle_key_bits(int preset) {
+  if (is_k3(preset)) return 3;
+  if (preset == PRESET_K4V4_NC) return 4;
+  if (preset == PRESET_K2V4_NC) return 2;
+  return 0;
 }
 
 /* SplitMix64 (Steele, Lea and Flood; the output function as published by
@@ -89,10 +105,33 @@ int oracle_rs_sign(int j) { return (oracle_splitmix64(RS_SEED, (uint64_t)j) >> 6
 #define K3_S_OFF 1824
 #define K3_Z_OFF 1856
 #define K3_PAGE 1920
+/* k4v4_nc slot = 64 + 2 + 64 + 2 + 2 = 134 B and k2v4_nc slot = 32 + 2 + 64 +
+ * 2 + 2 = 102 B, each rounded up to a multiple of 4 bytes like k3v4_nc's
+ * (136 B and 104 B): the same planar page, 32 B of padding at the end */
+#define K4_PAGE 2176
+#define K2_PAGE 1664
+
+/* Offsets of the planar page of a coded-key preset: codes [16][code_bytes]
+ * @0, key factor fp16 [16], value codes [128][8], value scale fp16 [16],
+ * value zero fp16 [16]. */
+typedef struct {
+  int code_bytes, nc_off, v_off, s_off, z_off, page;
+} coded_layout;
+
+static coded_layout coded_page(int preset) {
+  coded_layout l;
+  l.code_bytes = D * oracle_key_bits(preset) / 8;
+  l.nc_off = BLK * l.code_bytes;
+  l.v_off = l.nc_off + 2 * BLK;
+  l.s_off = l.v_off + BLK * D / 2;
+  l.z_off = l.s_off + 2 * BLK;
+  l.page = preset == PRESET_K4V4_NC ? K4_PAGE : preset == PRESET_K2V4_NC ? K2_PAGE : K3_PAGE;
+  return l;
+}
 
 long oracle_page_bytes(int preset) {
   if (preset == PRESET_K8V4) return K8_PAGE;
-  if (is_k3(preset)) return K3_PAGE;
+  if (oracle_key_bits(preset) > 0) return coded_page(preset).page;
   return -1;
 }
 
@@ -186,23 +225,24 @@ static double norm_quantile(double p) { /* bisection on the CDF */
   return 0.5 * (lo + hi);
 }
 
-/* 8-level Lloyd-Max quantiser of the standard normal, fp64.  Lloyd's two
- * conditions are iterated from the equiprobable quantile midpoints: every
- * decision boundary is the midpoint of its two neighbouring levels, and every
- * level is the conditional mean of N(0,1) over its cell,
+/* n-level Lloyd-Max quantiser of the standard normal, fp64 (n <= 16).
+ * Lloyd's two conditions are iterated from the equiprobable quantile
+ * midpoints: every decision boundary is the midpoint of its two neighbouring
+ * levels, and every level is the conditional mean of N(0,1) over its cell,
  *   c = (phi(a) - phi(b)) / (Q(a) - Q(b)).
  * Returns the iteration count, or -1 if it did not converge.  ([SD] "Context":
  * a precomputed Lloyd-Max codebook for the rotated key coordinates.) */
-int oracle_lloyd_max8(double c_out[8]) {
-  double c[8];
-  for (int m = 0; m < 8; ++m) c[m] = norm_quantile((m + 0.5) / 8.0);
+int oracle_lloyd_max(int n, double* c_out) {
+  double c[16];
+  if (n < 2 || n > 16) return -1;
+  for (int m = 0; m < n; ++m) c[m] = norm_quantile((m + 0.5) / n);
   for (int it = 1; it <= 200000; ++it) {
-    double b[9];
+    double b[17];
     b[0] = -INFINITY;
-    b[8] = INFINITY;
-    for (int m = 0; m < 7; ++m) b[m + 1] = 0.5 * (c[m] + c[m + 1]);
+    b[n] = INFINITY;
+    for (int m = 0; m < n - 1; ++m) b[m + 1] = 0.5 * (c[m] + c[m + 1]);
     double delta = 0.0;
-    for (int m = 0; m < 8; ++m) {
+    for (int m = 0; m < n; ++m) {
       double lo = b[m], hi = b[m + 1];
       double pa = isinf(lo) ? 0.0 : phi(lo), pb = isinf(hi) ? 0.0 : phi(hi);
       double qa = isinf(lo) ? 1.0 : qtail(lo), qb = isinf(hi) ? 0.0 : qtail(hi);
@@ -212,22 +252,33 @@ int oracle_lloyd_max8(double c_out[8]) {
       c[m] = nc;
     }
     if (delta < 1e-15) {
-      memcpy(c_out, c, sizeof c);
+      memcpy(c_out, c, n * sizeof(double));
       return it;
     }
   }
-  memcpy(c_out, c, sizeof c);
+  memcpy(c_out, c, n * sizeof(double));
   return -1;
 }
 
-/* The key codebook of preset k3v4_nc: Lloyd-Max levels for N(0, 1/D) rounded
- * to fp16 (ascending).  Returned as fp16 bit patterns. */
-int oracle_codebook16(uint16_t out[8]) {
-  double c[8];
-  int it = oracle_lloyd_max8(c);
+int oracle_lloyd_max8(double c_out[8]) { return oracle_lloyd_max(8, c_out); }
+
+/* The key codebook of an n-level preset: Lloyd-Max levels for N(0, 1/D)
+ * rounded to fp16 (ascending).  Returned as fp16 bit patterns. */
+int oracle_codebook_n(int n, uint16_t* out) {
+  double c[16];
+  int it = oracle_lloyd_max(n, c);
   double sigma = 1.0 / sqrt((double)D);
-  for (int m = 0; m < 8; ++m) out[m] = oracle_d2h_rn(c[m] * sigma);
+  for (int m = 0; m < n; ++m) out[m] = oracle_d2h_rn(c[m] * sigma);
   return it;
+}
+
+/* The 8-level codebook of the k3 presets. */
+int oracle_codebook16(uint16_t out[8]) { return oracle_codebook_n(8, out); }
+
+/* Number of key levels of a preset (0 for k8v4). */
+int oracle_key_levels(int preset) {
+  int b = oracle_key_bits(preset);
+  return b ? 1 << b : 0;
 }
 
 /* -------------------------------------------------------------- encoder */
@@ -270,49 +321,55 @@ float oracle_tree_sum(const float a[D]) {
   return p[0];
 }
 
-/* Index of the cell of y: the number of decision boundaries strictly below y
- * (a tie goes to the lower cell). */
-int oracle_quant_index(float y, const uint16_t cb[8]) {
+/* Index of the cell of y in an n-level codebook: the number of decision
+ * boundaries strictly below y (a tie goes to the lower cell). */
+int oracle_quant_index_n(float y, const uint16_t* cb, int n) {
   int idx = 0;
-  for (int m = 0; m < 7; ++m) {
+  for (int m = 0; m < n - 1; ++m) {
     float bm = (oracle_h2f(cb[m]) + oracle_h2f(cb[m + 1])) / 2.0f;
     if (y > bm) ++idx;
   }
   return idx;
 }
 
-/* 3-bit codes, LSB-first: bit (3j + b) of the 48-byte little-endian stream is
- * bit b of idx[j]. */
-void oracle_pack3(const uint8_t idx[D], uint8_t out[48]) {
-  memset(out, 0, 48);
+int oracle_quant_index(float y, const uint16_t cb[8]) { return oracle_quant_index_n(y, cb, 8); }
+
+/* b-bit codes, LSB-first: bit (b j + i) of the (b D / 8)-byte little-endian
+ * stream is bit i of idx[j]. */
+void oracle_pack_bits(const uint8_t idx[D], int bits, uint8_t* out) {
+  memset(out, 0, D * bits / 8);
   for (int j = 0; j < D; ++j)
-    for (int b = 0; b < 3; ++b)
+    for (int b = 0; b < bits; ++b)
       if ((idx[j] >> b) & 1) {
-        int bit = 3 * j + b;
+        int bit = bits * j + b;
         out[bit >> 3] |= (uint8_t)(1u << (bit & 7));
       }
 }
 
-void oracle_unpack3(const uint8_t in[48], uint8_t idx[D]) {
+void oracle_unpack_bits(const uint8_t* in, int bits, uint8_t idx[D]) {
   for (int j = 0; j < D; ++j) {
     int v = 0;
-    for (int b = 0; b < 3; ++b) {
-      int bit = 3 * j + b;
+    for (int b = 0; b < bits; ++b) {
+      int bit = bits * j + b;
       v |= ((in[bit >> 3] >> (bit & 7)) & 1) << b;
     }
     idx[j] = (uint8_t)v;
   }
 }
 
+void oracle_pack3(const uint8_t idx[D], uint8_t out[48]) { oracle_pack_bits(idx, 3, out); }
+void oracle_unpack3(const uint8_t in[48], uint8_t idx[D]) { oracle_unpack_bits(in, 3, idx); }
+
 static void put_h(uint8_t* p, uint16_t h) { p[0] = (uint8_t)(h & 255); p[1] = (uint8_t)(h >> 8); }
 static uint16_t get_h(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
 
-/* k3 key encoder for one token-head: norm, rotation, nearest centroid, bit
- * packing, and the fp16 key factor: |k| / |c_hat| (norm correction, preset
- * k3v4_nc) when corrected, else |k| (preset k3v4).  Writes 48 code bytes and
- * the factor. */
-void oracle_encode_key3_factor(const uint16_t k[D], const uint16_t cb[8], uint8_t codes[48],
-                               uint16_t* nc_out, int corrected, int signed_rotation) {
+/* Coded-key encoder for one token-head with an n-level codebook (n = 2^bits):
+ * norm, rotation, nearest centroid, bit packing, and the fp16 key factor:
+ * |k| / |c_hat| (norm correction, the _nc presets) when corrected, else |k|
+ * (preset k3v4).  Writes D bits / 8 code bytes and the factor. */
+void oracle_encode_keyq(const uint16_t k[D], const uint16_t* cb, int bits, uint8_t* codes,
+                        uint16_t* nc_out, int corrected, int signed_rotation) {
+  int n = 1 << bits;
   float x[D], sq[D], t[D];
   for (int j = 0; j < D; ++j) {
     x[j] = oracle_h2f(k[j]);
@@ -327,14 +384,19 @@ void oracle_encode_key3_factor(const uint16_t k[D], const uint16_t cb[8], uint8_
   float c2[D];
   for (int j = 0; j < D; ++j) {
     float y = (norm == 0.0f) ? 0.0f : t[j] / denom;
-    idx[j] = (uint8_t)oracle_quant_index(y, cb);
+    idx[j] = (uint8_t)oracle_quant_index_n(y, cb, n);
     float c = oracle_h2f(cb[idx[j]]);
     c2[j] = c * c;
   }
   float cn2 = oracle_tree_sum(c2);
   if (!corrected) *nc_out = oracle_f2h_rn(norm);
   else *nc_out = (norm == 0.0f) ? 0 : oracle_f2h_rn(norm / sqrtf(cn2));
-  oracle_pack3(idx, codes);
+  oracle_pack_bits(idx, bits, codes);
+}
+
+void oracle_encode_key3_factor(const uint16_t k[D], const uint16_t cb[8], uint8_t codes[48],
+                               uint16_t* nc_out, int corrected, int signed_rotation) {
+  oracle_encode_keyq(k, cb, 3, codes, nc_out, corrected, signed_rotation);
 }
 
 /* k3v4_nc key encoder (norm correction). */
@@ -401,8 +463,9 @@ int oracle_store(int preset, uint8_t* cache, int num_blocks, int Hk, const uint1
                  const uint16_t* v, const int32_t* slot_mapping, int T) {
   long pb = oracle_page_bytes(preset);
   if (pb < 0) return -1;
-  uint16_t cb[8];
-  if (is_k3(preset)) oracle_codebook16(cb);
+  uint16_t cb[16];
+  int bits = oracle_key_bits(preset);
+  if (bits) oracle_codebook_n(1 << bits, cb);
   /* heads own disjoint pages, so they can be encoded in parallel; tokens of
    * one head share value-code bytes and are encoded in order */
 #pragma omp parallel for schedule(static)
@@ -423,13 +486,14 @@ int oracle_store(int preset, uint8_t* cache, int num_blocks, int Hk, const uint1
         put_h(page + K8_S_OFF + 2 * off, s);
         put_h(page + K8_Z_OFF + 2 * off, z);
       } else {
+        coded_layout l = coded_page(preset);
         uint16_t nc;
-        oracle_encode_key3_factor(kk, cb, page + K3_K_OFF + off * 48, &nc, preset != PRESET_K3V4,
-                                  preset == PRESET_K3V4_NC_RS);
-        put_h(page + K3_NC_OFF + 2 * off, nc);
-        put_value_codes(page + K3_V_OFF, off, code);
-        put_h(page + K3_S_OFF + 2 * off, s);
-        put_h(page + K3_Z_OFF + 2 * off, z);
+        oracle_encode_keyq(kk, cb, bits, page + off * l.code_bytes, &nc, preset != PRESET_K3V4,
+                           preset == PRESET_K3V4_NC_RS);
+        put_h(page + l.nc_off + 2 * off, nc);
+        put_value_codes(page + l.v_off, off, code);
+        put_h(page + l.s_off + 2 * off, s);
+        put_h(page + l.z_off + 2 * off, z);
       }
     }
   }
@@ -441,17 +505,18 @@ int oracle_store(int preset, uint8_t* cache, int num_blocks, int Hk, const uint1
 /* Decoded key of one cached token, fp64.  k8v4: the e4m3 value.  k3v4_nc:
  * k_hat = nc * H c_hat / sqrt(D) (H / sqrt(D) is symmetric and orthonormal, so
  * this inverts the rotation of the encoder). */
-void oracle_decode_key(int preset, const uint8_t* page, int off, const uint16_t cb[8],
+void oracle_decode_key(int preset, const uint8_t* page, int off, const uint16_t* cb,
                        double out[D]) {
   if (preset == PRESET_K8V4) {
     for (int j = 0; j < D; ++j) out[j] = oracle_e4m3_to_double(page[K8_K_OFF + off * D + j]);
     return;
   }
+  coded_layout l = coded_page(preset);
   uint8_t idx[D];
-  oracle_unpack3(page + K3_K_OFF + off * 48, idx);
+  oracle_unpack_bits(page + off * l.code_bytes, oracle_key_bits(preset), idx);
   for (int j = 0; j < D; ++j) out[j] = (double)oracle_h2f(cb[idx[j]]);
   oracle_wht_f64(out);
-  double nc = (double)oracle_h2f(get_h(page + K3_NC_OFF + 2 * off));
+  double nc = (double)oracle_h2f(get_h(page + l.nc_off + 2 * off));
   for (int j = 0; j < D; ++j) out[j] = nc * out[j] / sqrt((double)D);
   /* k3v4_nc_rs: the encoder rotated by H diag(s), whose inverse is diag(s) H / D */
   if (preset == PRESET_K3V4_NC_RS)
@@ -460,9 +525,10 @@ void oracle_decode_key(int preset, const uint8_t* page, int off, const uint16_t 
 
 /* Decoded value: v_hat = code * scale + zero, fp64. */
 void oracle_decode_value(int preset, const uint8_t* page, int off, double out[D]) {
-  int vo = preset == PRESET_K8V4 ? K8_V_OFF : K3_V_OFF;
-  int so = preset == PRESET_K8V4 ? K8_S_OFF : K3_S_OFF;
-  int zo = preset == PRESET_K8V4 ? K8_Z_OFF : K3_Z_OFF;
+  coded_layout l = coded_page(preset);
+  int vo = preset == PRESET_K8V4 ? K8_V_OFF : l.v_off;
+  int so = preset == PRESET_K8V4 ? K8_S_OFF : l.s_off;
+  int zo = preset == PRESET_K8V4 ? K8_Z_OFF : l.z_off;
   double s = (double)oracle_h2f(get_h(page + so + 2 * off));
   double z = (double)oracle_h2f(get_h(page + zo + 2 * off));
   for (int j = 0; j < D; ++j) out[j] = (double)get_value_code(page + vo, off, j) * s + z;
@@ -481,7 +547,7 @@ typedef struct {
   int max_blocks;
   const uint16_t* raw_k;
   const uint16_t* raw_v;
-  uint16_t cb[8];
+  uint16_t cb[16];
 } kv_source;
 
 /* Returns 0 and fills out, or -1 when the position's block id is invalid. */
@@ -599,7 +665,7 @@ static void make_source(kv_source* src, int preset, const uint8_t* cache, int nu
   src->g = g;
   src->bt = bt_row;
   src->max_blocks = max_blocks;
-  if (is_k3(preset)) oracle_codebook16(src->cb);
+  if (oracle_key_bits(preset)) oracle_codebook_n(oracle_key_levels(preset), src->cb);
 }
 
 /* Spec-verify attention for a list of output rows.  Each row is (n, b, h):
