@@ -34,7 +34,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "µs per spec-verify call and achieved HBM GB/s vs peak (k8v4, k3v4_nc)"
-CONFIG_INDEX = {"tiny_k8v4": 0, "poc_k8v4": 1, "poc_k3v4_nc": 2, "decode_k3v4_nc": 3, "longctx_k3v4_nc": 4}
+# seed offsets: the five configurations in order, then the PoC shape with the
+# other key widths
+CONFIG_INDEX = {"tiny_k8v4": 0, "poc_k8v4": 1, "poc_k3v4_nc": 2, "decode_k3v4_nc": 3, "longctx_k3v4_nc": 4,
+                "poc_k4v4_nc": 5, "poc_k2v4_nc": 6}
 
 
 def parse_args():

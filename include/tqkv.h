@@ -61,9 +61,14 @@ typedef enum {
                              correction |k| / |c_hat|; values 4-bit            */
   TQ_PRESET_K3V4 = 2,     /* as k3v4_nc (same page), but the fp16 key factor is
                              the plain norm |k| (no correction)                */
-  TQ_PRESET_K3V4_NC_RS = 3 /* as k3v4_nc, keys rotated by H diag(s) / sqrt(128):
+  TQ_PRESET_K3V4_NC_RS = 3, /* as k3v4_nc, keys rotated by H diag(s) / sqrt(128):
                              s_j = -1 where the top bit of output j of
                              SplitMix64 seeded 0x54515F5349474E53 is set      */
+  TQ_PRESET_K4V4_NC = 4,  /* as k3v4_nc with 4-bit codes of the 16-level
+                             Lloyd-Max codebook (the "3-4 bit" widths of the
+                             "Context" section)                                */
+  TQ_PRESET_K2V4_NC = 5   /* as k3v4_nc with 2-bit codes of the 4-level
+                             Lloyd-Max codebook                                */
 } tq_preset;
 
 /* Description of a caller-owned paged cache in device memory.
@@ -74,10 +79,16 @@ typedef enum {
  *   k3v4_nc (1920 B = 16 x 120): K codes [16][48] @0 | K nc fp16 [16] @768
  *           | V codes [128][8] @800 | V scale fp16 [16] @1824
  *           | V zero fp16 [16] @1856 | 32 B padding @1888 (never written)
- * V codes are coordinate-major: byte 8d + t/2 holds the 4-bit code of
- * coordinate d for token t of the page (low nibble for even t).  The 3-bit
- * key codes of a token form a little-endian bit stream, code j at bits
- * 3j..3j+2.
+ *   k4v4_nc (2176 B = 16 x 136): K codes [16][64] @0 | K nc fp16 [16] @1024
+ *           | V codes [128][8] @1056 | V scale @2080 | V zero @2112
+ *           | 32 B padding @2144
+ *   k2v4_nc (1664 B = 16 x 104): K codes [16][32] @0 | K nc fp16 [16] @512
+ *           | V codes [128][8] @544 | V scale @1568 | V zero @1600
+ *           | 32 B padding @1632
+ * (k3v4 and k3v4_nc_rs use the k3v4_nc page.)  V codes are coordinate-major:
+ * byte 8d + t/2 holds the 4-bit code of coordinate d for token t of the page
+ * (low nibble for even t).  The b-bit key codes of a token (b = 3, 4, 2) form
+ * a little-endian bit stream, code j at bits bj..bj+b-1.
  * `cache` must be 16-byte aligned. */
 typedef struct {
   int32_t preset;       /* tq_preset                                  */
@@ -89,21 +100,27 @@ typedef struct {
   void* cache;          /* device pointer, see layout above           */
 } tq_cache_desc;
 
-/* Bytes of one (block, kv-head) page: 3136 (k8v4), 1920 (k3v4_nc), 0 for an
- * unknown preset.  16 x the slot size of the "Roofline" section (196 B for
- * k8v4; 120 B for k3v4_nc). */
+/* Bytes of one (block, kv-head) page: 3136 (k8v4), 1920 (k3 presets), 2176
+ * (k4v4_nc), 1664 (k2v4_nc), 0 for an unknown preset.  16 x the slot size of
+ * the "Roofline" section (196 B for k8v4; 120 B for k3v4_nc; the other widths
+ * rounded up to 4 bytes the same way). */
 size_t tq_page_bytes(int32_t preset);
+
+/* Levels of a preset's key codebook: 8 (k3 presets), 16 (k4v4_nc), 4
+ * (k2v4_nc), 0 for k8v4 or an unknown preset. */
+int32_t tq_key_levels(int32_t preset);
 
 /* Bytes of the stage-1 partials for one call: partial_o (fp32
  * [n_spec][B][Hq][num_kv_splits][128]) plus partial_lse (fp32
  * [n_spec][B][Hq][num_kv_splits]).  0 if an argument is < 1. */
 size_t tq_partials_bytes(int32_t n_spec, int32_t B, int32_t Hq, int32_t num_kv_splits);
 
-/* The k3v4_nc key codebook: the 8-level Lloyd-Max quantiser of N(0, 1/128)
- * ("Context" section: a precomputed Lloyd-Max codebook), derived in fp64 at
- * first use and rounded to fp16; written ascending to the HOST array
- * centroids_out[8] as the fp32 values of those fp16 numbers.  Returns
- * TQ_ERR_UNSUPPORTED for k8v4 (no codebook), TQ_ERR_INVALID_ARG for NULL. */
+/* A preset's key codebook: the n-level Lloyd-Max quantiser of N(0, 1/128),
+ * n = tq_key_levels(preset) ("Context" section: a precomputed Lloyd-Max
+ * codebook), derived in fp64 at first use and rounded to fp16; written
+ * ascending to the HOST array centroids_out[n] as the fp32 values of those
+ * fp16 numbers.  Returns TQ_ERR_UNSUPPORTED for k8v4 (no codebook),
+ * TQ_ERR_INVALID_ARG for NULL or an unknown preset. */
 tq_status tq_codebook(int32_t preset, float* centroids_out);
 
 /* Static English text for a status code (never NULL). */

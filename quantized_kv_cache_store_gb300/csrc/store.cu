@@ -58,10 +58,7 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
     const uint16_t vh[4] = {(uint16_t)(vr.x & 0xFFFF), (uint16_t)(vr.x >> 16), (uint16_t)(vr.y & 0xFFFF),
                             (uint16_t)(vr.y >> 16)};
     if (run8) {
-      if (PRESET == 0)
-        store_ops::store_key8(page, off, lane, kh);
-      else
-        store_ops::store_key3(page, off, lane, kh, a.cb, a.plain_norm == 0, store_ops::lane_signs(a.signs, lane));
+      store_ops::store_key<PRESET>(page, off, lane, kh, a.cb, a.plain_norm == 0, store_ops::lane_signs(a.signs, lane));
       uint32_t c[4];
       store_ops::value4_codes<L>(page, off, lane, vh, c);
 #pragma unroll
@@ -87,8 +84,12 @@ cudaError_t launch_store(int preset, const StoreArgs& a, cudaStream_t st) {
   if (units == 0) return cudaSuccess;
   const unsigned grid = (unsigned)units;
   // the k3 presets differ only in runtime flags (a.plain_norm, a.signs)
-  return preset == 0 ? launch_pdl(store_kernel<0>, dim3(grid), dim3(256), 0, st, a)
-                      : launch_pdl(store_kernel<1>, dim3(grid), dim3(256), 0, st, a);
+  switch (preset) {
+    case 0: return launch_pdl(store_kernel<0>, dim3(grid), dim3(256), 0, st, a);
+    case 4: return launch_pdl(store_kernel<4>, dim3(grid), dim3(256), 0, st, a);
+    case 5: return launch_pdl(store_kernel<5>, dim3(grid), dim3(256), 0, st, a);
+    default: return launch_pdl(store_kernel<1>, dim3(grid), dim3(256), 0, st, a);
+  }
 }
 
 }  // namespace tq

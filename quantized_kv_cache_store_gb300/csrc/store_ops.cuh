@@ -10,7 +10,8 @@
 //            rounds at lane offsets 16, 8, 4, 2, 1;
 //   H k    = unnormalised Sylvester butterflies, stride 1, 2 in-lane, then
 //            strides 4..64 across lanes (offset stride / 4), (a + b, a - b);
-//   y      = (H k) / (|k| * sqrt(128)),  code = #{boundaries strictly below y};
+//   y      = (H k) / (|k| * sqrt(128)),  code = #{boundaries strictly below y}
+//            (7, 15 or 3 boundaries: 3-, 4- or 2-bit codes);
 //   nc     = fp16(|k| / sqrt(|c_hat|^2)) with |c_hat|^2 summed in the same order.
 #pragma once
 
@@ -52,11 +53,14 @@ __device__ __forceinline__ void store_key8(uint8_t* page, int off, int lane, con
   *reinterpret_cast<uint32_t*>(page + K8::kKey + off * kD + 4 * lane) = w;
 }
 
-// k3 keys; the fp16 key factor is |k| / |c_hat| (norm correction, k3v4_nc)
-// when corrected, else |k| (k3v4); bit i of signs flips the lane's coordinate
-// i before the rotation (randomised-sign Hadamard, k3v4_nc_rs)
-__device__ __forceinline__ void store_key3(uint8_t* page, int off, int lane, const uint16_t h[4],
+// coded keys, BITS = 3, 4 or 2 per coordinate (2^BITS-level codebook, page
+// layout L); the fp16 key factor is |k| / |c_hat| (norm correction, the _nc
+// presets) when corrected, else |k| (k3v4); bit i of signs flips the lane's
+// coordinate i before the rotation (randomised-sign Hadamard, k3v4_nc_rs)
+template <class L, int BITS>
+__device__ __forceinline__ void store_keyq(uint8_t* page, int off, int lane, const uint16_t h[4],
                                            const Codebook& cb, bool corrected = true, uint32_t signs = 0u) {
+  constexpr int N = 1 << BITS;
   float x[4], t[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -94,11 +98,11 @@ __device__ __forceinline__ void store_key3(uint8_t* page, int off, int lane, con
       t[i] = upper ? __fsub_rn(p, t[i]) : __fadd_rn(t[i], p);
     }
   }
-  float C[8], Bd[7];
+  float C[N], Bd[N - 1];
 #pragma unroll
-  for (int m = 0; m < 8; ++m) C[m] = half_bits_to_float(cb.c[m]);
+  for (int m = 0; m < N; ++m) C[m] = half_bits_to_float(cb.c[m]);
 #pragma unroll
-  for (int m = 0; m < 7; ++m) Bd[m] = __fmul_rn(__fadd_rn(C[m], C[m + 1]), 0.5f);
+  for (int m = 0; m < N - 1; ++m) Bd[m] = __fmul_rn(__fadd_rn(C[m], C[m + 1]), 0.5f);
   const float denom = __fmul_rn(norm, __fsqrt_rn(128.0f));
   uint32_t code[4];
   float c2[4];
@@ -107,35 +111,42 @@ __device__ __forceinline__ void store_key3(uint8_t* page, int off, int lane, con
     const float y = (norm == 0.0f) ? 0.0f : __fdiv_rn(t[i], denom);
     uint32_t idx = 0;
 #pragma unroll
-    for (int m = 0; m < 7; ++m) idx += (y > Bd[m]) ? 1u : 0u;
+    for (int m = 0; m < N - 1; ++m) idx += (y > Bd[m]) ? 1u : 0u;
     code[i] = idx;
     float c = C[0];
 #pragma unroll
-    for (int m = 1; m < 8; ++m) c = (idx == (uint32_t)m) ? C[m] : c;
+    for (int m = 1; m < N; ++m) c = (idx == (uint32_t)m) ? C[m] : c;
     c2[i] = __fmul_rn(c, c);
   }
   const float cn2 = tree_sum(c2[0], c2[1], c2[2], c2[3]);
-  // 12 bits per lane at stream bit 12 * lane; 48 bytes = 12 little-endian words
-  const uint32_t bits = code[0] | (code[1] << 3) | (code[2] << 6) | (code[3] << 9);
-  const int w = lane;  // output word handled by lanes 0..11
-  uint64_t word = 0;
-  const int first = (32 * w) / 12;
+  // 4 BITS bits per lane at stream bit 4 BITS lane of the token's 16 BITS bytes
+  const uint32_t bits = code[0] | (code[1] << BITS) | (code[2] << (2 * BITS)) | (code[3] << (3 * BITS));
+  uint8_t* kcodes = page + L::kKey + off * (16 * BITS);
+  if constexpr (BITS == 4) {
+    *reinterpret_cast<uint16_t*>(kcodes + 2 * lane) = (uint16_t)bits;
+  } else if constexpr (BITS == 2) {
+    kcodes[lane] = (uint8_t)bits;
+  } else {
+    // 12 bits per lane: 48 bytes = 12 little-endian words, word w gathered by lane w
+    const int w = lane;
+    uint64_t word = 0;
+    const int first = (32 * w) / 12;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int src = min(first + j, 31);
-    const uint32_t val = __shfl_sync(kFull, bits, src);
-    const int shift = 12 * src - 32 * w;  // position of src's bits inside this word
-    if (first + j <= 31 && shift > -12 && shift < 32) {
-      word |= shift >= 0 ? ((uint64_t)val << shift) : ((uint64_t)val >> (-shift));
+    for (int j = 0; j < 4; ++j) {
+      const int src = min(first + j, 31);
+      const uint32_t val = __shfl_sync(kFull, bits, src);
+      const int shift = 12 * src - 32 * w;  // position of src's bits inside this word
+      if (first + j <= 31 && shift > -12 && shift < 32) {
+        word |= shift >= 0 ? ((uint64_t)val << shift) : ((uint64_t)val >> (-shift));
+      }
     }
+    if (lane < 12) *reinterpret_cast<uint32_t*>(kcodes + 4 * w) = (uint32_t)(word & 0xFFFFFFFFull);
   }
-  if (lane < 12)
-    *reinterpret_cast<uint32_t*>(page + K3::kKey + off * 48 + 4 * w) = (uint32_t)(word & 0xFFFFFFFFull);
   if (lane == 0) {
     const uint16_t nc = !corrected ? __half_as_ushort(__float2half_rn(norm))
                         : (norm == 0.0f) ? (uint16_t)0
                                          : __half_as_ushort(__float2half_rn(__fdiv_rn(norm, __fsqrt_rn(cn2))));
-    *reinterpret_cast<uint16_t*>(page + K3::kNc + 2 * off) = nc;
+    *reinterpret_cast<uint16_t*>(page + L::kNc + 2 * off) = nc;
   }
 }
 
@@ -203,15 +214,22 @@ __device__ __forceinline__ uint32_t lane_signs(const uint32_t signs[4], int lane
   return (signs[lane >> 3] >> (4 * (lane & 7))) & 0xFu;
 }
 
+// the key of one (token, kv-head) for a kernel preset (0: FP8, else coded)
+template <int PRESET>
+__device__ __forceinline__ void store_key(uint8_t* page, int off, int lane, const uint16_t kh[4], const Codebook& cb,
+                                          bool corrected, uint32_t signs) {
+  if constexpr (PRESET == 0)
+    store_key8(page, off, lane, kh);
+  else
+    store_keyq<Layout<PRESET>, key_bits<PRESET>()>(page, off, lane, kh, cb, corrected, signs);
+}
+
 template <int PRESET>
 __device__ __forceinline__ void store_token(uint8_t* page, int off, int lane, const uint16_t kh[4],
                                             const uint16_t vh[4], const Codebook& cb, bool plain_norm = PRESET == 2,
                                             uint32_t signs = 0u) {
   using L = Layout<PRESET>;
-  if (PRESET == 0)
-    store_key8(page, off, lane, kh);
-  else
-    store_key3(page, off, lane, kh, cb, !plain_norm, signs);
+  store_key<PRESET>(page, off, lane, kh, cb, !plain_norm, signs);
   store_value4<L>(page, off, lane, vh);
 }
 

@@ -30,6 +30,27 @@ struct K3 {
   static constexpr int kPage = 1920;  // 32 B padding at 1888
 };
 
+// the other key widths: 4-bit (16-level) and 2-bit (4-level) codes, the
+// k3v4_nc page with slots of 134 B and 102 B rounded up to 4 bytes
+struct K4 {
+  static constexpr int kKey = 0;      // 4-bit codes [16][64]
+  static constexpr int kNc = 1024;    // fp16 [16]
+  static constexpr int kVal = 1056;   // codes [128 coord][8 B: 16 tokens]
+  static constexpr int kScale = 2080; // fp16 [16]
+  static constexpr int kZero = 2112;  // fp16 [16]
+  static constexpr int kPage = 2176;  // 32 B padding at 2144
+};
+struct K2 {
+  static constexpr int kKey = 0;      // 2-bit codes [16][32]
+  static constexpr int kNc = 512;     // fp16 [16]
+  static constexpr int kVal = 544;    // codes [128 coord][8 B: 16 tokens]
+  static constexpr int kScale = 1568; // fp16 [16]
+  static constexpr int kZero = 1600;  // fp16 [16]
+  static constexpr int kPage = 1664;  // 32 B padding at 1632
+};
+
+// Kernel presets: 0 = k8v4, 1 = the k3 presets (k3v4_nc, k3v4, k3v4_nc_rs
+// differ in runtime flags only), 4 = k4v4_nc, 5 = k2v4_nc.
 template <int PRESET>
 struct Layout;
 template <>
@@ -39,10 +60,21 @@ struct Layout<1> : K3 {};
 // k3v4: k3v4_nc's page, the plain norm |k| as key factor
 template <>
 struct Layout<2> : K3 {};
+template <>
+struct Layout<4> : K4 {};
+template <>
+struct Layout<5> : K2 {};
 
-// Eight fp16 centroids, ascending, passed to kernels by value.
+// bits per key code (0: FP8 keys)
+template <int PRESET>
+__host__ __device__ constexpr int key_bits() {
+  return PRESET == 0 ? 0 : PRESET == 4 ? 4 : PRESET == 5 ? 2 : 3;
+}
+
+// Up to sixteen fp16 centroids, ascending (8 for the k3 presets, 16 for
+// k4v4_nc, 4 for k2v4_nc), passed to kernels by value.
 struct Codebook {
-  uint16_t c[8];
+  uint16_t c[16];
 };
 
 struct StoreArgs {

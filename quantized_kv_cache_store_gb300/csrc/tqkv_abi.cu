@@ -11,16 +11,16 @@ namespace {
 
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
-// 8-level Lloyd-Max quantiser of the standard normal (fp64): alternate the
-// nearest-neighbour condition (thresholds at midpoints of adjacent levels)
-// and the centroid condition (each level is the mean of N(0,1) over its
-// interval: (pdf(lo) - pdf(hi)) / (cdf(hi) - cdf(lo))) until no level moves
-// by more than 1e-15.  The levels for N(0, 1/128) are these times 1/sqrt(128),
-// rounded to fp16 ("spec-decode-intel-arc", section "Context": keys are coded
-// against a precomputed Lloyd-Max codebook).
-tq::Codebook derive_codebook() {
-  double y[8];
-  for (int i = 0; i < 8; ++i) y[i] = -1.75 + 0.5 * i;  // uniform start
+// n-level Lloyd-Max quantiser of the standard normal (fp64, n = 4, 8, 16):
+// alternate the nearest-neighbour condition (thresholds at midpoints of
+// adjacent levels) and the centroid condition (each level is the mean of
+// N(0,1) over its interval: (pdf(lo) - pdf(hi)) / (cdf(hi) - cdf(lo))) until
+// no level moves by more than 1e-15.  The levels for N(0, 1/128) are these
+// times 1/sqrt(128), rounded to fp16 ("spec-decode-intel-arc", section
+// "Context": keys are coded against a precomputed Lloyd-Max codebook).
+tq::Codebook derive_codebook(int n) {
+  double y[16];
+  for (int i = 0; i < n; ++i) y[i] = -2.0 + 4.0 * (i + 0.5) / n;  // uniform start
   auto pdf = [](double x) { return std::isinf(x) ? 0.0 : std::exp(-0.5 * x * x) * 0.3989422804014327; };
   auto cdf = [](double x) {
     if (std::isinf(x)) return x > 0 ? 1.0 : 0.0;
@@ -31,12 +31,12 @@ tq::Codebook derive_codebook() {
     return 0.5 * std::erfc(x * 0.7071067811865476);
   };
   for (int iter = 0; iter < 1000000; ++iter) {
-    double t[9];
+    double t[17];
     t[0] = -INFINITY;
-    t[8] = INFINITY;
-    for (int i = 1; i < 8; ++i) t[i] = 0.5 * (y[i - 1] + y[i]);
+    t[n] = INFINITY;
+    for (int i = 1; i < n; ++i) t[i] = 0.5 * (y[i - 1] + y[i]);
     double moved = 0.0;
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < n; ++i) {
       const double lo = t[i], hi = t[i + 1];
       // probability mass of the cell, from whichever tail keeps precision
       const double mass = (lo >= 0.0) ? sf(lo) - sf(hi) : cdf(hi) - cdf(lo);
@@ -46,14 +46,28 @@ tq::Codebook derive_codebook() {
     }
     if (moved < 1e-15) break;
   }
-  tq::Codebook cb;
-  for (int i = 0; i < 8; ++i) cb.c[i] = __half_as_ushort(__double2half(y[i] / std::sqrt(128.0)));
+  tq::Codebook cb = {};
+  for (int i = 0; i < n; ++i) cb.c[i] = __half_as_ushort(__double2half(y[i] / std::sqrt(128.0)));
   return cb;
 }
 
-const tq::Codebook& codebook() {
-  static const tq::Codebook cb = derive_codebook();  // thread-safe one-time init
-  return cb;
+// levels of a preset's key codebook (0: FP8 keys or unknown)
+int key_levels(int32_t preset) {
+  switch (preset) {
+    case TQ_PRESET_K3V4_NC:
+    case TQ_PRESET_K3V4:
+    case TQ_PRESET_K3V4_NC_RS: return 8;
+    case TQ_PRESET_K4V4_NC: return 16;
+    case TQ_PRESET_K2V4_NC: return 4;
+    default: return 0;
+  }
+}
+
+// the codebook of a coded-key preset (thread-safe one-time init per size)
+const tq::Codebook& codebook(int32_t preset) {
+  static const tq::Codebook c8 = derive_codebook(8), c16 = derive_codebook(16), c4 = derive_codebook(4);
+  const int n = key_levels(preset);
+  return n == 16 ? c16 : n == 4 ? c4 : c8;
 }
 
 // The sign vector of preset k3v4_nc_rs, as a mask (bit j set: s_j = -1):
@@ -82,13 +96,15 @@ bool is_k3(int32_t preset) {
 size_t page_bytes(int32_t preset) {
   if (preset == TQ_PRESET_K8V4) return tq::K8::kPage;
   if (is_k3(preset)) return tq::K3::kPage;
+  if (preset == TQ_PRESET_K4V4_NC) return tq::K4::kPage;
+  if (preset == TQ_PRESET_K2V4_NC) return tq::K2::kPage;
   return 0;
 }
 
 tq_status check_desc(const tq_cache_desc* d) {
   if (!d || !d->cache) return TQ_ERR_INVALID_ARG;
   if (d->num_kv_heads < 1 || d->num_blocks < 0 || d->reserved != 0) return TQ_ERR_INVALID_ARG;
-  if (d->preset != TQ_PRESET_K8V4 && !is_k3(d->preset)) return TQ_ERR_UNSUPPORTED;
+  if (page_bytes(d->preset) == 0) return TQ_ERR_UNSUPPORTED;
   if (d->head_dim != 128 || d->block_size != 16) return TQ_ERR_UNSUPPORTED;
   if (d->num_kv_heads > 65535) return TQ_ERR_UNSUPPORTED;
   if (!aligned(d->cache, 16)) return TQ_ERR_MISALIGNED;
@@ -142,7 +158,7 @@ tq_status verify_args(const tq_cache_desc* cache, const void* q, const int32_t* 
     const SignMask m = rs_signs(cache->preset);
     for (int i = 0; i < 4; ++i) a.signs[i] = m.w[i];
   }
-  a.cb = codebook();
+  a.cb = codebook(cache->preset);
   return TQ_OK;
 }
 
@@ -157,11 +173,14 @@ size_t tq_partials_bytes(int32_t n_spec, int32_t B, int32_t Hq, int32_t num_kv_s
   return (size_t)n_spec * (size_t)B * (size_t)Hq * (size_t)num_kv_splits * (128 + 1) * sizeof(float);
 }
 
+int32_t tq_key_levels(int32_t preset) { return key_levels(preset); }
+
 tq_status tq_codebook(int32_t preset, float* centroids_out) {
   if (!centroids_out) return TQ_ERR_INVALID_ARG;
-  if (!is_k3(preset)) return preset == TQ_PRESET_K8V4 ? TQ_ERR_UNSUPPORTED : TQ_ERR_INVALID_ARG;
-  const tq::Codebook& cb = codebook();
-  for (int i = 0; i < 8; ++i) centroids_out[i] = __half2float(__ushort_as_half(cb.c[i]));
+  const int n = key_levels(preset);
+  if (n == 0) return preset == TQ_PRESET_K8V4 ? TQ_ERR_UNSUPPORTED : TQ_ERR_INVALID_ARG;
+  const tq::Codebook& cb = codebook(preset);
+  for (int i = 0; i < n; ++i) centroids_out[i] = __half2float(__ushort_as_half(cb.c[i]));
   return TQ_OK;
 }
 
@@ -203,7 +222,7 @@ tq_status tq_store(const tq_cache_desc* cache, const void* k, const void* v, con
     const SignMask m = rs_signs(cache->preset);
     for (int i = 0; i < 4; ++i) a.signs[i] = m.w[i];
   }
-  a.cb = codebook();
+  a.cb = codebook(cache->preset);
   return from_cuda(tq::launch_store(cache->preset, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -278,7 +297,7 @@ tq_status tq_store_verify(const tq_cache_desc* cache, const void* k_new, const v
   sa.n_spec = n_spec;
   sa.plain_norm = a.plain_norm;
   for (int i = 0; i < 4; ++i) sa.signs[i] = a.signs[i];
-  sa.cb = codebook();
+  sa.cb = codebook(cache->preset);
   s = from_cuda(tq::launch_store(cache->preset, sa, st));
   if (s != TQ_OK) return s;
   return tq_verify(cache, q, block_table, max_blocks, seq_lens, n_spec, B, Hq, num_kv_splits, causal, partial_o,

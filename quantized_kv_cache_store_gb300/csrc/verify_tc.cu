@@ -90,7 +90,11 @@ struct Cfg {
   static constexpr int kRestBytes = L::kPage - kKeyBlock;
   static constexpr int kRestOff = kPages * kKeyBlock;
   static constexpr int kStageBytes = align_up(kPages * L::kPage, 1024);
-  static constexpr int kStages = PRESET == 0 ? 5 : 8;
+  static constexpr int kStages = PRESET == 0 ? 5 : PRESET == 4 ? 6 : 8;
+  static constexpr int kKeyBits = key_bits<PRESET>();  // 0: FP8 keys
+  // code-pair table: entry e = (code of coordinate 2j) | (code of 2j+1) << bits,
+  // replicated for the 32 lanes
+  static constexpr int kPairEntries = PRESET == 0 ? 0 : 1 << (2 * kKeyBits);
   static constexpr int kSW = NR == 64 ? 2 : 1;    // softmax warpgroups
   static constexpr int kRS = NR == 64 ? 32 : NR;  // query rows per softmax thread
   static constexpr int kThreads = 256 + 128 * kSW;
@@ -119,8 +123,8 @@ struct Cfg {
   // yet (bit mask) @512
   static constexpr int kRed = kCol + 4 * kTok * 16;
   static constexpr int kRedWG = 4096;
-  static constexpr int kPair = kRed + kSW * kRedWG;  // u32 [64][32] (k3v4_nc)
-  static constexpr int kPValid = kPair + (PRESET == 1 ? 64 * 32 * 4 : 0);  // u8 [kStages][8]
+  static constexpr int kPair = kRed + kSW * kRedWG;  // u32 [kPairEntries][32] (coded keys)
+  static constexpr int kPValid = kPair + kPairEntries * 32 * 4;  // u8 [kStages][8]
   static constexpr int kBar = align_up(kPValid + kStages * 8, 8);
   // full[kStages] empty[kStages] ak[4] sready[2] pfull[3] pv[3] sfree[2] av[3]
   static constexpr int kProducers = 3;  // warps 0, 2, 3 copy pages 0-2, 3-5, 6-7 of a chunk
@@ -437,7 +441,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
           x[8 * u + 2 * e + 1] = __high2float(h2);
         }
       }
-      if (PRESET == 1) {
+      if (PRESET != 0) {
         // signs of coordinates 32 part + e, then the butterflies of strides
         // 1 .. 16 in the thread and 32, 64 across the row's four threads
         const uint32_t sg = a.signs[q_part];
@@ -475,10 +479,11 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
                        pack_half2(x[8 * hc + 4], x[8 * hc + 5]), pack_half2(x[8 * hc + 6], x[8 * hc + 7]));
       }
     }
-    if (PRESET == 1) {
-      for (int i = tid - 128; i < 64 * 32; i += C::kThreads - 128) {
+    if (PRESET != 0) {
+      constexpr int kB = C::kKeyBits, kLv = 1 << kB;
+      for (int i = tid - 128; i < C::kPairEntries * 32; i += C::kThreads - 128) {
         const int e = i >> 5;
-        pairs[i] = (uint32_t)a.cb.c[e & 7] | ((uint32_t)a.cb.c[e >> 3] << 16);
+        pairs[i] = (uint32_t)a.cb.c[e & (kLv - 1)] | ((uint32_t)a.cb.c[e >> kB] << 16);
       }
     }
   }
@@ -665,27 +670,30 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
           tmem_st32(ak + 32 * h, r);
         }
       } else {
-        // 384 bits of 3-bit codes; pair j (coordinates 2j, 2j+1) at bits 6j .. 6j+5
-        const uint4* kw = reinterpret_cast<const uint4*>(stage + pg_i * L::kPage + L::kKey + off_i * 48);
-        uint32_t wd[13];
+        // 128 b-bit codes (b = 3, 4, 2): 16 b bytes; pair j (coordinates
+        // 2j, 2j+1) at stream bits 2bj .. 2bj + 2b - 1
+        constexpr int kB2 = 2 * C::kKeyBits, kW = 4 * C::kKeyBits;  // pair bits, code words
+        const uint4* kw =
+            reinterpret_cast<const uint4*>(stage + pg_i * L::kPage + L::kKey + off_i * (16 * C::kKeyBits));
+        uint32_t wd[kW + 1];
 #pragma unroll
-        for (int u = 0; u < 3; ++u) {
+        for (int u = 0; u < kW / 4; ++u) {
           const uint4 w = kw[u];
           wd[4 * u + 0] = w.x;
           wd[4 * u + 1] = w.y;
           wd[4 * u + 2] = w.z;
           wd[4 * u + 3] = w.w;
         }
-        wd[12] = 0u;
+        wd[kW] = 0u;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t r[32];
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
-            const int bit = 6 * (32 * h + jj), wi = bit >> 5, sh = bit & 31;
+            const int bit = kB2 * (32 * h + jj), wi = bit >> 5, sh = bit & 31;
             uint32_t f = wd[wi] >> sh;
-            if (sh > 26) f |= wd[wi + 1] << (32 - sh);
-            r[jj] = pairs[(f & 63u) * 32 + lane];
+            if (sh > 32 - kB2) f |= wd[wi + 1] << (32 - sh);
+            r[jj] = pairs[(f & ((1u << kB2) - 1u)) * 32 + lane];
           }
           tmem_st32(ak + 32 * h, r);
         }
@@ -698,7 +706,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         int rmin = 1 << 20;
         if (valid) {
           const uint8_t* pg = pgf(st, pg_i);
-          if constexpr (PRESET == 1)
+          if constexpr (PRESET != 0)
             cs = __half2float(*reinterpret_cast<const __half*>(pg + L::kNc + 2 * off_i)) * sl2;
           // odd tokens enter the value operand 16 times larger
           sv = __half2float(*reinterpret_cast<const __half*>(pg + L::kScale + 2 * off_i)) * ((i & 1) ? 0.0625f : 1.f);
@@ -1261,15 +1269,33 @@ int fused_capacity() {
 }  // namespace
 
 
-cudaError_t launch_verify_stage1_tc(int preset, const VerifyArgs& a, cudaStream_t st) {
-  if (preset == 0) {
-    if (a.R <= 16) return launch_tc<0, 16, false>(a, st);
-    if (a.R <= 32) return launch_tc<0, 32, false>(a, st);
-    return launch_tc<0, 64, false>(a, st);
+// kernel preset of a cache preset: the k3 presets share one kernel
+int kernel_preset(int preset) { return preset == 0 || preset == 4 || preset == 5 ? preset : 1; }
+
+template <int P, bool FUSED>
+cudaError_t launch_rows(const VerifyArgs& a, cudaStream_t st) {
+  if (a.R <= 16) return launch_tc<P, 16, FUSED>(a, st);
+  if (a.R <= 32) return launch_tc<P, 32, FUSED>(a, st);
+  return launch_tc<P, 64, FUSED>(a, st);
+}
+
+template <bool FUSED>
+cudaError_t launch_preset(int preset, const VerifyArgs& a, cudaStream_t st) {
+  switch (kernel_preset(preset)) {
+    case 0: return launch_rows<0, FUSED>(a, st);
+    case 4: return launch_rows<4, FUSED>(a, st);
+    case 5: return launch_rows<5, FUSED>(a, st);
+    default: return launch_rows<1, FUSED>(a, st);
   }
-  if (a.R <= 16) return launch_tc<1, 16, false>(a, st);
-  if (a.R <= 32) return launch_tc<1, 32, false>(a, st);
-  return launch_tc<1, 64, false>(a, st);
+}
+
+template <int P>
+int capacity_rows(const VerifyArgs& a) {
+  return a.R <= 16 ? fused_capacity<P, 16>() : a.R <= 32 ? fused_capacity<P, 32>() : fused_capacity<P, 64>();
+}
+
+cudaError_t launch_verify_stage1_tc(int preset, const VerifyArgs& a, cudaStream_t st) {
+  return launch_preset<false>(preset, a, st);
 }
 
 bool verify_fused_supported(int preset, const VerifyArgs& a) {
@@ -1277,20 +1303,17 @@ bool verify_fused_supported(int preset, const VerifyArgs& a) {
   // every CTA resident at once (the merge waits for all splits)
   const long ctas = (long)a.S * a.Hk * a.B * a.rtiles;
   int cap = 0;
-  if (preset == 0) cap = a.R <= 16 ? fused_capacity<0, 16>() : a.R <= 32 ? fused_capacity<0, 32>() : fused_capacity<0, 64>();
-  else cap = a.R <= 16 ? fused_capacity<1, 16>() : a.R <= 32 ? fused_capacity<1, 32>() : fused_capacity<1, 64>();
+  switch (kernel_preset(preset)) {
+    case 0: cap = capacity_rows<0>(a); break;
+    case 4: cap = capacity_rows<4>(a); break;
+    case 5: cap = capacity_rows<5>(a); break;
+    default: cap = capacity_rows<1>(a); break;
+  }
   return ctas <= cap;
 }
 
 cudaError_t launch_verify_fused(int preset, const VerifyArgs& a, cudaStream_t st) {
-  if (preset == 0) {
-    if (a.R <= 16) return launch_tc<0, 16, true>(a, st);
-    if (a.R <= 32) return launch_tc<0, 32, true>(a, st);
-    return launch_tc<0, 64, true>(a, st);
-  }
-  if (a.R <= 16) return launch_tc<1, 16, true>(a, st);
-  if (a.R <= 32) return launch_tc<1, 32, true>(a, st);
-  return launch_tc<1, 64, true>(a, st);
+  return launch_preset<true>(preset, a, st);
 }
 
 cudaError_t read_device_error(unsigned int* out, bool clear) {

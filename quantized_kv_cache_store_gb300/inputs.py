@@ -27,13 +27,13 @@ import torch
 
 HEAD_DIM = 128
 BLOCK = 16
-PRESETS = {"k8v4": 0, "k3v4_nc": 1, "k3v4": 2, "k3v4_nc_rs": 3}
+PRESETS = {"k8v4": 0, "k3v4_nc": 1, "k3v4": 2, "k3v4_nc_rs": 3, "k4v4_nc": 4, "k2v4_nc": 5}
 
 
 @dataclass(frozen=True)
 class Workload:
     name: str
-    preset: str            # "k8v4" | "k3v4_nc" | "k3v4" | "k3v4_nc_rs"
+    preset: str            # "k8v4" | "k3v4_nc" | "k3v4" | "k3v4_nc_rs" | "k4v4_nc" | "k2v4_nc"
     n_spec: int
     B: int
     Hq: int
@@ -72,6 +72,11 @@ WORKLOADS = {
                                len_range=(1024, 32768), num_kv_splits=4, shuffled_blocks=True),
     "longctx_k3v4_nc": Workload("longctx_k3v4_nc", "k3v4_nc", n_spec=8, B=2, Hq=32, Hk=4,
                                 seq_len=262144, num_kv_splits=19, k_scale=(0.5, 2.0)),
+    # the PoC shape with the other key widths (4-bit and 2-bit codes)
+    "poc_k4v4_nc": Workload("poc_k4v4_nc", "k4v4_nc", n_spec=8, B=4, Hq=32, Hk=4, seq_len=8192,
+                            num_kv_splits=8),
+    "poc_k2v4_nc": Workload("poc_k2v4_nc", "k2v4_nc", n_spec=8, B=4, Hq=32, Hk=4, seq_len=8192,
+                            num_kv_splits=8),
 }
 
 

@@ -26,8 +26,10 @@ TQ_PRESET_K8V4 = 0
 TQ_PRESET_K3V4_NC = 1
 TQ_PRESET_K3V4 = 2
 TQ_PRESET_K3V4_NC_RS = 3
+TQ_PRESET_K4V4_NC = 4
+TQ_PRESET_K2V4_NC = 5
 PRESETS = {"k8v4": TQ_PRESET_K8V4, "k3v4_nc": TQ_PRESET_K3V4_NC, "k3v4": TQ_PRESET_K3V4,
-           "k3v4_nc_rs": TQ_PRESET_K3V4_NC_RS}
+           "k3v4_nc_rs": TQ_PRESET_K3V4_NC_RS, "k4v4_nc": TQ_PRESET_K4V4_NC, "k2v4_nc": TQ_PRESET_K2V4_NC}
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +71,8 @@ def load(build_if_missing: bool = False):
         lib.tq_partials_bytes.argtypes = [I, I, I, I]
         lib.tq_codebook.restype = I
         lib.tq_codebook.argtypes = [I, P]
+        lib.tq_key_levels.restype = I
+        lib.tq_key_levels.argtypes = [I]
         lib.tq_status_string.restype = ctypes.c_char_p
         lib.tq_status_string.argtypes = [I]
         D = ctypes.POINTER(tq_cache_desc)
@@ -123,8 +127,12 @@ def tq_partials_bytes(n_spec: int, B: int, Hq: int, num_kv_splits: int) -> int:
     return int(load().tq_partials_bytes(n_spec, B, Hq, num_kv_splits))
 
 
+def tq_key_levels(preset: int) -> int:
+    return int(load().tq_key_levels(int(preset)))
+
+
 def tq_codebook(preset: int = TQ_PRESET_K3V4_NC) -> np.ndarray:
-    out = np.zeros(8, np.float32)
+    out = np.zeros(max(tq_key_levels(preset), 1), np.float32)
     _check(load().tq_codebook(int(preset), ctypes.c_void_p(out.ctypes.data)), "tq_codebook")
     return out
 

@@ -36,6 +36,7 @@ def test_exports_every_declared_symbol(lib):
 def test_page_and_partials_bytes(lib):
     assert tqkv.tq_page_bytes(0) == 3136 and tqkv.tq_page_bytes(1) == 1920 and tqkv.tq_page_bytes(2) == 1920
     assert tqkv.tq_page_bytes(3) == 1920
+    assert tqkv.tq_page_bytes(4) == 2176 and tqkv.tq_page_bytes(5) == 1664
     assert tqkv.tq_page_bytes(7) == 0
     assert tqkv.tq_partials_bytes(8, 4, 32, 8) == 8 * 4 * 32 * 8 * 129 * 4
     assert tqkv.tq_partials_bytes(0, 4, 32, 8) == 0
@@ -51,6 +52,11 @@ def test_codebook_matches_oracle(lib, oracle_lib):
     ours = tqkv.tq_codebook(1)
     ref = oracle_lib.codebook16().view(np.float16).astype(np.float32)
     assert np.array_equal(ours, ref)
+    for preset, n in ((2, 8), (3, 8), (4, 16), (5, 4)):
+        assert tqkv.tq_key_levels(preset) == n == oracle_lib.key_levels(preset)
+        ref = oracle_lib.codebook_n(n).view(np.float16).astype(np.float32)
+        assert np.array_equal(tqkv.tq_codebook(preset), ref)
+    assert tqkv.tq_key_levels(0) == 0 and tqkv.tq_key_levels(9) == 0
     out = np.zeros(8, np.float32)
     assert lib.tq_codebook(0, ctypes.c_void_p(out.ctypes.data)) == tqkv.TQ_ERR_UNSUPPORTED
     assert lib.tq_codebook(1, None) == tqkv.TQ_ERR_INVALID_ARG
@@ -74,7 +80,7 @@ def test_store_validation(lib):
                                                              P(s), T, None)
     assert st(None) == tqkv.TQ_ERR_INVALID_ARG
     assert st(_desc(ptr=0)) == tqkv.TQ_ERR_INVALID_ARG
-    assert st(_desc(preset=5, ptr=FAKE)) == tqkv.TQ_ERR_UNSUPPORTED
+    assert st(_desc(preset=6, ptr=FAKE)) == tqkv.TQ_ERR_UNSUPPORTED
     assert st(_desc(head_dim=64, ptr=FAKE)) == tqkv.TQ_ERR_UNSUPPORTED
     assert st(_desc(block=32, ptr=FAKE)) == tqkv.TQ_ERR_UNSUPPORTED
     assert st(_desc(hk=0, ptr=FAKE)) == tqkv.TQ_ERR_INVALID_ARG
@@ -152,7 +158,8 @@ def test_header_enums_match_the_binding():
     text = open(HEADER).read()
     decl = {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(TQ_[A-Z0-9_]+)\s*=\s*(\d+)", text)}
     for name in ("TQ_OK", "TQ_ERR_INVALID_ARG", "TQ_ERR_UNSUPPORTED", "TQ_ERR_MISALIGNED", "TQ_ERR_CUDA",
-                 "TQ_ERR_TIMEOUT", "TQ_PRESET_K8V4", "TQ_PRESET_K3V4_NC", "TQ_PRESET_K3V4", "TQ_PRESET_K3V4_NC_RS"):
+                 "TQ_ERR_TIMEOUT", "TQ_PRESET_K8V4", "TQ_PRESET_K3V4_NC", "TQ_PRESET_K3V4", "TQ_PRESET_K3V4_NC_RS",
+                 "TQ_PRESET_K4V4_NC", "TQ_PRESET_K2V4_NC"):
         assert decl[name] == getattr(tqkv, name), name
     assert tqkv.PRESETS == inputs.PRESETS
     for preset in tqkv.PRESETS.values():

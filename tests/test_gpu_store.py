@@ -25,7 +25,7 @@ def _store_both(O, preset, k, v, slots, nb, hk):
     return cache.cpu().numpy(), ref
 
 
-@pytest.mark.parametrize("preset", [0, 1, 2, 3])
+@pytest.mark.parametrize("preset", [0, 1, 2, 3, 4, 5])
 @pytest.mark.parametrize("seed", [42, 101, 202])
 def test_store_random_ragged(oracle_lib, preset, seed):
     rng = np.random.default_rng(seed)
@@ -40,7 +40,7 @@ def test_store_random_ragged(oracle_lib, preset, seed):
     assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("preset", [0, 1, 2, 3])
+@pytest.mark.parametrize("preset", [0, 1, 2, 3, 4, 5])
 def test_store_special_values(oracle_lib, preset):
     hk, T = 1, 8
     k = np.zeros((T, hk, 128), np.float16)

@@ -29,8 +29,11 @@ CASES = [
                        num_kv_splits=2)),                                # ragged, shuffled pages
     ("tiny_k8v4", dict(n_spec=3, B=2, Hq=2, Hk=2, seq_len=3, num_kv_splits=4)),  # no cached prefix
     ("tiny_k8v4", dict(n_spec=2, B=3, Hq=8, Hk=4, seq_len=700, num_kv_splits=40)),  # two launches
+    ("tiny_k8v4", dict(preset="k4v4_nc", n_spec=8, B=2, Hq=16, Hk=2, seq_len=500, num_kv_splits=3)),
+    ("tiny_k8v4", dict(preset="k2v4_nc", n_spec=16, B=1, Hq=4, Hk=1, seq_len=200, num_kv_splits=4)),
     ("poc_k8v4", {}),
     ("poc_k3v4_nc", {}),
+    ("poc_k3v4_nc", dict(preset="k4v4_nc")),
 ]
 
 

@@ -41,9 +41,16 @@ SMALL = [
     ("k3v4", 8, 2, 4, 2, 203, 3, True),     # plain-norm preset
     ("k3v4", 1, 3, 8, 2, (17, 300), 4, False),
     ("k3v4_nc_rs", 8, 2, 4, 2, 203, 3, True),  # randomised-sign Hadamard
-    ("k3v4_nc_rs", 16, 1, 8, 1, 100, 5, True),  # 128 rows: the mma.sync stage 1
+    ("k3v4_nc_rs", 16, 1, 8, 1, 100, 5, True),  # 128 rows: two row tiles
     ("k3v4_nc", 2, 1, 16, 1, 77, 2, True),
     ("k3v4_nc", 16, 1, 16, 2, 190, 3, True),  # 128 rows per kv-head
+    ("k4v4_nc", 8, 1, 8, 1, 256, 2, True),    # the other key widths
+    ("k2v4_nc", 8, 1, 8, 1, 256, 2, True),
+    ("k4v4_nc", 8, 2, 4, 2, 203, 3, False),
+    ("k2v4_nc", 1, 5, 32, 8, (1, 90), 2, True),
+    ("k4v4_nc", 1, 3, 8, 2, (17, 300), 4, True),
+    ("k2v4_nc", 16, 1, 16, 2, 190, 3, True),
+    ("k4v4_nc", 4, 2, 8, 1, 300, 3, True),
 ]
 
 
@@ -247,8 +254,8 @@ def test_unused_slots_with_garbage_do_not_leak():
     assert torch.equal(out, ref)
 
 
-# ---- tq_verify: both stages in one call (one launch with a cluster merge for
-# R <= 64 and S in 1..4, 6, 8; else stage 1 + stage 2)
+# ---- tq_verify: both stages in one call (one launch whose splits merge through
+# per-pair counters when every CTA is resident and S <= 32; else stage 1 + stage 2)
 
 FUSED = [
     # (preset, n_spec, B, Hq, Hk, seq_len / len_range, S, causal)
@@ -266,7 +273,10 @@ FUSED = [
     ("k3v4_nc_rs", 8, 1, 32, 4, 555, 7, True),
     ("k8v4", 1, 2, 8, 1, 2000, 32, True),   # the most splits one launch merges
     ("k8v4", 2, 3, 8, 4, 700, 40, False),   # more splits than one launch merges: two launches
-    ("k8v4", 16, 1, 8, 1, 100, 3, True),    # 128 rows: mma.sync stage 1 + stage 2
+    ("k8v4", 16, 1, 8, 1, 100, 3, True),    # 128 rows: two row tiles in one launch
+    ("k4v4_nc", 8, 1, 32, 4, 555, 7, True),
+    ("k2v4_nc", 8, 2, 16, 2, 900, 6, True),
+    ("k4v4_nc", 16, 1, 16, 2, 190, 3, True),
 ]
 
 
@@ -310,7 +320,7 @@ def test_single_call_verify_poc(oracle_lib, name):
 # section: chunks of up to 128 query tokens take the spec-verify path): up to
 # 1024 query rows per kv-head, tiled 64 rows per CTA on the tensor cores.
 
-@pytest.mark.parametrize("preset", ["k8v4", "k3v4_nc"])
+@pytest.mark.parametrize("preset", ["k8v4", "k3v4_nc", "k4v4_nc", "k2v4_nc"])
 @pytest.mark.parametrize("q_len,group,L,S", [(16, 8, 300, 3), (64, 4, 700, 2), (128, 8, 600, 2), (128, 2, 1500, 5)])
 def test_continuation_chunks_match_oracle(oracle_lib, preset, q_len, group, L, S):
     from quantized_kv_cache_store_gb300.step import SpecVerify
