@@ -161,9 +161,11 @@ tq_status tq_store(const tq_cache_desc* cache, const void* k, const void* v,
  * each (n, b, h, s): partial_o = softmax-weighted mean of the decoded values
  * over the visible positions of the split, partial_lse = ln(sum exp(score))
  * with score = q . k_hat / sqrt(128); an empty range gives partial_o = 0 and
- * partial_lse = -inf.  Requires 1 <= n_spec <= 16, Hq % num_kv_heads == 0,
- * n_spec * Hq / num_kv_heads <= 128, 1 <= num_kv_splits <= 65535,
- * B <= 65535. */
+ * partial_lse = -inf.  Requires 1 <= n_spec <= 128, Hq % num_kv_heads == 0,
+ * R = n_spec * Hq / num_kv_heads <= 1024 (the rows of one kv-head: up to 16
+ * drafts at GQA 8, or a continuation chunk of up to 128 query tokens; rows
+ * beyond 64 are tiled 64 per CTA over the same pages), 1 <= num_kv_splits <=
+ * 65535, B * ceil(R / 64) <= 65535; otherwise TQ_ERR_UNSUPPORTED. */
 tq_status tq_verify_stage1(const tq_cache_desc* cache, const void* q, const int32_t* block_table,
                            int32_t max_blocks, const int32_t* seq_lens, int32_t n_spec, int32_t B,
                            int32_t Hq, int32_t num_kv_splits, int32_t causal, float* partial_o,
@@ -184,21 +186,23 @@ tq_status tq_verify_stage2(const float* partial_o, const float* partial_lse, int
  * query head, as tq_verify_stage1 followed by tq_verify_stage2 (the
  * split-KV partial attention, "sycl-three-attempts-arc-b70" section "Part 3",
  * and its log-sum-exp merge).  The pages run the two stages as two launches.
- * Here, when n_spec * Hq / Hk <= 64, num_kv_splits <= 32 and all
- * num_kv_splits * Hk * B CTAs fit on the device at once, one cooperative
- * launch runs both: every split writes its partial rows, counts itself in
- * on a per-(sequence, kv-head) counter, waits (bounded) until all splits of
- * that pair have, then merges its share of the rows (split s: rows
- * [s r, (s + 1) r), r = ceil(R / S)).  Otherwise stage 1 and stage 2 are
+ * Here, when num_kv_splits <= 32 and all num_kv_splits * Hk * B *
+ * ceil(R / 64) CTAs fit on the device at once, one cooperative launch runs
+ * both: every CTA (split s, row tile t of its (sequence, kv-head) pair;
+ * unit u = t S + s) writes its partial rows, counts itself in on the pair's
+ * arrival counter, waits (bounded) until all S ceil(R / 64) CTAs of the pair
+ * have, then merges its share of the rows (rows [u r, (u + 1) r),
+ * r = ceil(R / (S ceil(R / 64)))).  Otherwise stage 1 and stage 2 are
  * enqueued as two launches.
  * Arguments, layouts, alignment and validation are those of
  * tq_verify_stage1 (its first twelve arguments; the partials are scratch
  * here and their contents unspecified afterwards) plus
  *   tickets  u32 [B][Hk][4], 4-byte aligned, caller-owned: must be all zero
  *            before the first call and is all zero again after each call
- *            completes (entries 0 and 1 of each pair are its arrival and
- *            completion counters); calls that share a tickets buffer must not
- *            overlap in time (order them on one stream);
+ *            completes (entries 0, 1 and 2 of each pair are its arrival,
+ *            completion and stored-draft counters, entry 3 is unused); calls
+ *            that share a tickets buffer must not overlap in time (order them
+ *            on one stream);
  *   out      fp32 [n_spec][B][Hq][128], 16-byte aligned; written.
  * A cross-split wait that expires writes NaN rows and sets the device error
  * word (tq_device_status); the counters may then be left non-zero, so after
@@ -216,9 +220,12 @@ tq_status tq_verify(const tq_cache_desc* cache, const void* q, const int32_t* bl
  * of sequence b goes to position p = min(seq_lens[b], max_blocks * 16) -
  * n_spec + n, i.e. page block_table[b][p / 16], offset p % 16 (a negative p
  * or an out-of-range block id skips the draft), with the bytes tq_store
- * writes.  Where tq_verify runs as one launch, the CTA whose page range holds
- * a draft stores it before copying that page; otherwise a store launch and
- * tq_verify are enqueued.
+ * writes.  Where tq_verify runs as one launch, the drafts are stored inside
+ * it: CTA unit u of the pair stores drafts n = u mod (S ceil(R / 64)) while
+ * its first pages are in flight and counts them on the pair's draft counter
+ * (tickets entry 2); a CTA whose page range holds drafts copies those pages
+ * only after all n_spec are counted (bounded wait).  Otherwise a store launch
+ * and tq_verify are enqueued.
  * Arguments are those of tq_verify plus
  *   k_new, v_new  fp16 [B][n_spec][Hk][128], 16-byte aligned: the drafts'
  *                 keys and values (the cache is written, so it must not be
