@@ -102,7 +102,7 @@ struct Cfg {
   // softmax); their sum must stay within what the launch granted (checked at
   // launch: 128 registers a thread for 512 threads, 168 for 384)
   // (setmaxnreg is executed by all four warps of a warpgroup together)
-  static constexpr int kRegCtl = kSW == 2 ? 40 : 48;
+  static constexpr int kRegCtl = 48;
   static constexpr int kRegDq = 96;
   static constexpr int kRegSm = kSW == 2 ? 184 : 232;
   static constexpr int kRegNeeded = 128 * kRegCtl + 128 * kRegDq + 128 * kSW * kRegSm;
@@ -298,6 +298,26 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z / a.rtiles, rt = blockIdx.z % a.rtiles;
   const int row_off = rt * NR, Rt = min(a.R - row_off, NR);
   const int unit = rt * a.S + split;  // this CTA among the S x rtiles of its pair
+  // ---- set-up: barriers, tensor memory (warp 1, first thing: shared and
+  // tensor memory only, so it overlaps the wait for the previous grid)
+  if (tid == 32) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bars.full(s), C::kProducers);
+      mbar_init(bars.empty(s), 4);
+    }
+    for (int i = 0; i < 4; ++i) mbar_init(bars.ak(i), 4);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(bars.av(i), 4);
+      mbar_init(bars.pv(i), 1);
+      mbar_init(bars.pfull(i), 4 * C::kSW);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars.sready(i), 5);
+      mbar_init(bars.sfree(i), 4 * C::kSW);
+    }
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
   pdl_wait();
   pdl_trigger();
 
@@ -347,20 +367,18 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
   const int pw = warp == 0 ? 0 : warp - 1;
   const int p_lo = 3 * pw, p_hi = min(C::kPages, p_lo + 3);
   int ids = -1, ids_next = -1;  // this lane's block id for page 32 * (c / 4) + lane, and for the next group
+  // raw ids (validated when the page is copied, so that nothing waits for
+  // them before the set-up barrier)
   auto fetch_ids = [&](int c) -> int {
     const int lp = c * C::kPages + lane;
-    int id = -1;
-    if (lp < npages) {
-      id = bt[page_lo + lp];
-      id = (id >= 0 && id < a.num_blocks) ? id : -1;
-    }
-    return id;
+    return lp < npages ? bt[page_lo + lp] : -1;
   };
   // the cache pages are read once per call: evict them from L2 first
   const uint64_t pol = producer ? l2_evict_first() : 0ull;
   auto produce = [&](int c) {
     const int st = c % C::kStages;
-    const int mine = __shfl_sync(kFull, ids, (c & 3) * C::kPages + (lane & 7));
+    int mine = __shfl_sync(kFull, ids, (c & 3) * C::kPages + (lane & 7));
+    mine = (mine >= 0 && mine < a.num_blocks) ? mine : -1;
     const bool my = lane >= p_lo && lane < p_hi;
     const uint32_t nvalid = __popc(__ballot_sync(kFull, my && mine >= 0));
     // page flags first: the arrive below releases them to the consumers
@@ -387,25 +405,6 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     ids_next = fetch_ids(4);
   }
 
-  // ---- set-up: barriers, tensor memory (warp 1, which loads no block ids)
-  if (tid == 32) {
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bars.full(s), C::kProducers);
-      mbar_init(bars.empty(s), 4);
-    }
-    for (int i = 0; i < 4; ++i) mbar_init(bars.ak(i), 4);
-    for (int i = 0; i < 3; ++i) {
-      mbar_init(bars.av(i), 4);
-      mbar_init(bars.pv(i), 1);
-      mbar_init(bars.pfull(i), 4 * C::kSW);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bars.sready(i), 5);
-      mbar_init(bars.sfree(i), 4 * C::kSW);
-    }
-    *abort_flag = 0u;
-    fence_mbar_init();
-  }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
