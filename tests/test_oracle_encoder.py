@@ -52,6 +52,30 @@ def test_tree_sum_close_to_exact(oracle_lib):
     assert oracle_lib.tree_sum(ints) == float(ints.sum())
 
 
+def test_tree_sum_association_order(oracle_lib):
+    """The documented order, fixed by hand on inputs where fp32 rounding
+    (spacing 2 at 2^24, ties to even) tells the orders apart:
+    lane partials p_l = (a[4l] + a[4l+1]) + (a[4l+2] + a[4l+3]), then
+    p_l <- p_l + p_(l xor off) for off = 16, 8, 4, 2, 1."""
+    big = np.float32(2.0 ** 24)
+    # within a lane: (2^24 + 1) + (1 + 1) = 2^24 + 2 (the first sum ties to
+    # 2^24); left to right gives 2^24, right to left 2^24 + 4
+    a = np.zeros(D, np.float32)
+    a[0], a[1], a[2], a[3] = big, 1, 1, 1
+    assert oracle_lib.tree_sum(a) == 2.0 ** 24 + 2
+    # across lanes: lanes 1 and 17 meet first (offset 16) and give 2, added to
+    # lane 0's 2^24 last (offset 1): 2^24 + 2; with offset 1 first, each 1
+    # meets 2^24 alone and ties away: 2^24
+    a = np.zeros(D, np.float32)
+    a[0], a[4], a[68] = big, 1, 1
+    assert oracle_lib.tree_sum(a) == 2.0 ** 24 + 2
+    # offset 8 before offset 2: lanes 2 and 10 (1 each) meet at offset 8,
+    # then join lane 0 at offset 2
+    a = np.zeros(D, np.float32)
+    a[0], a[8], a[40] = big, 1, 1
+    assert oracle_lib.tree_sum(a) == 2.0 ** 24 + 2
+
+
 # ---------------------------------------------------------- centroid coding
 
 def test_quant_index_cells(oracle_lib):
