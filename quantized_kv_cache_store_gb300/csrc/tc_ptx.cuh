@@ -248,6 +248,10 @@ template <>
 __device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, uint32_t (&r)[16]) {
   tmem_ld16(taddr, r);
 }
+template <>
+__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, uint32_t (&r)[8]) {
+  tmem_ld8(taddr, r);
+}
 
 template <uint32_t R>
 __device__ __forceinline__ void regs_inc() {

@@ -73,9 +73,6 @@ constexpr uint32_t kSuspendNs = 20000;
 constexpr uint64_t kSpinNs = 500000000ull;
 constexpr uint32_t kSpinTries = 1u << 24;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
-// the MMA issuer polls its barriers without blocking; it gives up after
-// kSpinNs without progress (or kIssuerPolls idle polls)
-constexpr uint32_t kIssuerPolls = 1u << 26;
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -95,8 +92,16 @@ struct Cfg {
   // code-pair table: entry e = (code of coordinate 2j) | (code of 2j+1) << bits,
   // replicated for the 32 lanes
   static constexpr int kPairEntries = PRESET == 0 ? 0 : 1 << (2 * kKeyBits);
-  static constexpr int kSW = NR == 64 ? 2 : 1;    // softmax warpgroups
+  // two softmax warpgroups: with 64 rows each takes 32 rows of every chunk;
+  // with up to 32 rows each takes every row of alternate chunks (two
+  // streams, each with its own S^T buffers, O^T accumulator and running
+  // maximum, merged by log-sum-exp in the epilogue)
+  static constexpr int kSW = 2;
+  static constexpr int kStreams = NR == 64 ? 1 : 2;
   static constexpr int kRS = NR == 64 ? 32 : NR;  // query rows per softmax thread
+  static constexpr int kSbuf = 2 * kStreams;      // S^T buffers
+  // token-parameter slots (chunk c: c % kColP), at least kSbuf + 2 (a power of two)
+  static constexpr int kColP = kStreams == 2 ? 8 : 4;
   static constexpr int kThreads = 256 + 128 * kSW;
   // per-thread register budgets after setmaxnreg (control / dequant /
   // softmax); their sum must stay within what the launch granted (checked at
@@ -104,7 +109,7 @@ struct Cfg {
   // (setmaxnreg is executed by all four warps of a warpgroup together)
   static constexpr int kRegCtl = 48;
   static constexpr int kRegDq = 96;
-  static constexpr int kRegSm = kSW == 2 ? 184 : 232;
+  static constexpr int kRegSm = 184;
   static constexpr int kRegNeeded = 128 * kRegCtl + 128 * kRegDq + 128 * kSW * kRegSm;
   static_assert(kRegNeeded <= 65536, "register split exceeds the register file");
   static constexpr int kLine = 2 * NR;  // bytes of one P' line (one token)
@@ -116,28 +121,32 @@ struct Cfg {
   static constexpr int kQBytes = 2 * NR * 128;  // K-major, 128B swizzle, 2 x 64-coordinate blocks
   static constexpr int kP = kQ + align_up(kQBytes, 1024);
   static constexpr int kPBytes = kTok * kLine;  // one buffer
-  static constexpr int kCol = kP + 3 * kPBytes;  // float4 [4][128]: score scale, P' scale, v zero, first row
+  static constexpr int kCol = kP + 3 * kPBytes;  // float4 [kColP][128]: score scale, P' scale, v zero, first row
   // per softmax warpgroup (floats): -m [32] @0, rescale factors [32] @32,
   // row constants float2 [32] @64, per-warp row maxima [4][32] @128, per-warp
   // row sums of l and of the zero term [2][128] @256, rows without a maximum
   // yet (bit mask) @512
-  static constexpr int kRed = kCol + 4 * kTok * 16;
+  static constexpr int kRed = kCol + kColP * kTok * 16;
   static constexpr int kRedWG = 4096;
   static constexpr int kPair = kRed + kSW * kRedWG;  // u32 [kPairEntries][32] (coded keys)
   static constexpr int kPValid = kPair + kPairEntries * 32 * 4;  // u8 [kStages][8]
   static constexpr int kBar = align_up(kPValid + kStages * 8, 8);
-  // full[kStages] empty[kStages] ak[4] sready[2] pfull[3] pv[3] sfree[2] av[3]
-  static constexpr int kProducers = 3;  // warps 0, 2, 3 copy pages 0-2, 3-5, 6-7 of a chunk
-  static constexpr int kNumBars = 2 * kStages + 17;
+  // full[kStages] empty[kStages] ak[4] pfull[3] pv[3] av[3] pvs[2]
+  // sready[kSbuf] sfree[kSbuf]
+  // producers: warps 0, 2, 3 copy pages 0-2, 3-5, 6-7 of a chunk (64 rows,
+  // one MMA issuer); warps 2, 3 copy pages 0-3, 4-7 (two streams: warp 0
+  // issues the P.V MMAs)
+  static constexpr int kProducers = kStreams == 2 ? 2 : 3;
+  static constexpr int kNumBars = 2 * kStages + 15 + 2 * kSbuf;
   static constexpr int kMisc = kBar + 8 * kNumBars;  // u32 tmem base, u32 abort, u32 merge go
   static constexpr int kSmem = kMisc + 16 + 1024;    // + alignment slack
   // tensor memory columns
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTAK = 0;    // A_K[2]: 64 cols each (token lanes, coordinate pairs)
   static constexpr uint32_t kTAV = 128;  // A_V[3]: 64 cols each (coordinate lanes, token pairs)
-  static constexpr uint32_t kTS = 320;   // S^T[2]: NR cols each
-  static constexpr uint32_t kTO = 320 + 2 * NR;  // O^T: NR cols
-  static_assert(kTO + NR <= kTmemCols, "tensor memory overflow");
+  static constexpr uint32_t kTS = 320;   // S^T[kSbuf]: NR cols each
+  static constexpr uint32_t kTO = 320 + kSbuf * NR;  // O^T[kStreams]: NR cols each
+  static_assert(kTO + kStreams * NR <= kTmemCols, "tensor memory overflow");
   static_assert(kSmem <= 227 * 1024, "shared memory overflow");
 };
 
@@ -149,16 +158,20 @@ struct Cfg {
 struct Bars {
   uint32_t base;
   int stages;
+  int sbuf;  // S^T buffers
   __device__ uint32_t full(int s) const { return base + 8 * s; }
   __device__ uint32_t empty(int s) const { return base + 8 * (stages + s); }
   __device__ uint32_t ak(int i) const { return base + 8 * (2 * stages + i); }         // A_K + token params (c % 4)
-  // S^T = K Q^T done and chunk c's parameters written (c % 2): four dequant
-  // arrivals plus the issuer's commit, which also covers every earlier P.V
-  __device__ uint32_t sready(int b) const { return base + 8 * (2 * stages + 4 + b); }
-  __device__ uint32_t pfull(int i) const { return base + 8 * (2 * stages + 6 + i); }  // P' written (c % 3)
-  __device__ uint32_t pv(int i) const { return base + 8 * (2 * stages + 9 + i); }     // O^T += V^T P'^T done (c % 3)
-  __device__ uint32_t sfree(int b) const { return base + 8 * (2 * stages + 12 + b); } // S^T(c) read by the softmax (c % 2)
-  __device__ uint32_t av(int i) const { return base + 8 * (2 * stages + 14 + i); }    // A_V written (c % 3)
+  __device__ uint32_t pfull(int i) const { return base + 8 * (2 * stages + 4 + i); }  // P' written (c % 3)
+  __device__ uint32_t pv(int i) const { return base + 8 * (2 * stages + 7 + i); }     // O^T += V^T P'^T done (c % 3)
+  __device__ uint32_t av(int i) const { return base + 8 * (2 * stages + 10 + i); }    // A_V written (c % 3)
+  // P.V(c) done, per stream (c % 2; two-stream mode only)
+  __device__ uint32_t pvs(int j) const { return base + 8 * (2 * stages + 13 + j); }
+  // S^T = K Q^T done and chunk c's parameters written (c % sbuf): four
+  // dequant arrivals plus the issuer's commit, which also covers every
+  // earlier P.V
+  __device__ uint32_t sready(int b) const { return base + 8 * (2 * stages + 15 + b); }
+  __device__ uint32_t sfree(int b) const { return base + 8 * (2 * stages + 15 + sbuf + b); }  // S^T(c) read (c % sbuf)
 };
 
 __device__ __forceinline__ uint64_t now_ns() {
@@ -185,6 +198,26 @@ __device__ __forceinline__ bool spin_until_at_least(const uint32_t* counter, uin
   }
   atomicOr(&g_tq_device_error, 1u);
   return false;
+}
+
+// Bounded wait by polling (the MMA issuers: no suspension between polls);
+// false when the CTA aborted or this wait expired (which aborts).
+__device__ __forceinline__ bool poll_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if ((i & 63) == 63) {
+      const uint64_t t = now_ns();
+      if (t0 == 0) {
+        t0 = t;
+      } else if (t - t0 > kSpinNs || i >= (1u << 28)) {
+        *abort = 1u;
+        atomicOr(&g_tq_device_error, 1u);
+        return false;
+      }
+    }
+  }
 }
 
 // Bounded wait; false when the CTA aborted or this wait expired (which aborts).
@@ -289,7 +322,7 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
   uint32_t* pairs = reinterpret_cast<uint32_t*>(sm + C::kPair);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sm + C::kMisc + 4);
-  const Bars bars{sbase + C::kBar, C::kStages};
+  const Bars bars{sbase + C::kBar, C::kStages, C::kSbuf};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // rows beyond 64 per kv-head are tiled across CTAs: this CTA takes rows
@@ -306,14 +339,18 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       mbar_init(bars.empty(s), 4);
     }
     for (int i = 0; i < 4; ++i) mbar_init(bars.ak(i), 4);
+    // a chunk's S^T and P' are handled by both softmax warpgroups (64 rows)
+    // or by one (two streams)
+    constexpr int kPerChunk = 4 * C::kSW / C::kStreams;
     for (int i = 0; i < 3; ++i) {
       mbar_init(bars.av(i), 4);
       mbar_init(bars.pv(i), 1);
-      mbar_init(bars.pfull(i), 4 * C::kSW);
+      mbar_init(bars.pfull(i), kPerChunk);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 2; ++i) mbar_init(bars.pvs(i), 1);
+    for (int i = 0; i < C::kSbuf; ++i) {
       mbar_init(bars.sready(i), 5);
-      mbar_init(bars.sfree(i), 4 * C::kSW);
+      mbar_init(bars.sfree(i), kPerChunk);
     }
     *abort_flag = 0u;
     fence_mbar_init();
@@ -359,13 +396,15 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
   uint32_t* pair_tickets = FUSED ? a.tickets + ((long)b * a.Hk + kvh) * 4 : nullptr;
   const int32_t* bt = a.block_table + (long)b * a.max_blocks;
 
-  // Producers = warps 0, 2, 3 (C::kProducers): producer w copies pages
-  // [3 w, 3 w + 3) of each chunk, one page per lane, since a warp issues its
-  // lanes' copies one after another and each costs tens of cycles.  Block ids
-  // are fetched 32 pages (4 chunks) at a time, one id per lane, a group ahead.
-  const bool producer = warp == 0 || warp == 2 || warp == 3;
-  const int pw = warp == 0 ? 0 : warp - 1;
-  const int p_lo = 3 * pw, p_hi = min(C::kPages, p_lo + 3);
+  // Producers (C::kProducers: warps 0, 2, 3 or warps 2, 3): producer w copies
+  // pages [w ppw, (w + 1) ppw) of each chunk, one page per lane, since a warp
+  // issues its lanes' copies one after another and each costs tens of
+  // cycles.  Block ids are fetched 32 pages (4 chunks) at a time, one id per
+  // lane, a group ahead.
+  constexpr int kPpw = (C::kPages + C::kProducers - 1) / C::kProducers;  // pages per producer
+  const bool producer = warp == 2 || warp == 3 || (C::kProducers == 3 && warp == 0);
+  const int pw = C::kProducers == 3 ? (warp == 0 ? 0 : warp - 1) : warp - 2;
+  const int p_lo = kPpw * pw, p_hi = min(C::kPages, p_lo + kPpw);
   int ids = -1, ids_next = -1;  // this lane's block id for page 32 * (c / 4) + lane, and for the next group
   // raw ids (validated when the page is copied, so that nothing waits for
   // them before the set-up barrier)
@@ -556,70 +595,109 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       // drain: copies still in flight must land before the CTA can exit
       for (int cc = max(0, c - C::kStages); cc < c; ++cc)
         wait_bar(bars.full(cc % C::kStages), (cc / C::kStages) & 1, abort_flag, false);
-    } else if (warp == 1) {
-      // ================= MMA issuer (one thread), never blocked on one
-      // operand while the other kind of MMA could go: S^T(c) = K_hat(c) Q^T
-      // once softmax(c - 2) released its buffer and the keys of chunk c are in
-      // tensor memory; O^T += V^T P'^T(c) once softmax(c) wrote P'(c) and the
-      // values of chunk c are in tensor memory.  S^T(c) is issued only after
-      // P.V(c - 3): a commit tracks every earlier MMA of this thread, so the
-      // completion of S^T(c) then also means that P.V(c - 3) is done, which
-      // frees P' buffer c % 3 and value buffer c % 3 without a wait of their own.
-      if (lane == 0) {
-        constexpr uint32_t id_qk = idesc_f16(128, NR, 0, 0);
-        constexpr uint32_t id_pv = idesc_f16(128, NR, 0, 1);
-        constexpr uint32_t kQ1 = NR * 8;  // second 64-coordinate block of Q, in 16-byte units
-        constexpr uint32_t kL = C::kLine;  // P' line bytes: 16 lines per K-step
-        const uint64_t q_desc = smem_desc(sbase + C::kQ, 16, 1024, 2);
-        const uint64_t p_desc = smem_desc(sbase + C::kP, 16, 8 * C::kLine, C::kSwzMode);
-        int nq = 0, np = 0;
-        uint32_t idle = 0;
-        uint64_t idle_since = 0;  // time of the first idle poll since the last issue
-        while (np < nchunks) {
-          bool did = false;
-          if (nq < nchunks && nq - 3 < np &&
-              (nq < 2 || mbar_test_wait(bars.sfree(nq & 1), ((nq - 2) >> 1) & 1)) &&
-              mbar_test_wait(bars.ak(nq & 3), (nq >> 2) & 1)) {
-            tc_fence_after();
-            mma_ts_x8<2, 4, 6, kQ1, kQ1 + 2, kQ1 + 4, kQ1 + 6>(tmem + C::kTS + NR * (nq & 1),
-                                                               tmem + C::kTAK + 64 * (nq & 1), q_desc, id_qk, 0u);
-            tc_commit(bars.sready(nq & 1));
-            ++nq;
-            did = true;
-          }
-          if (np < nq && mbar_test_wait(bars.pfull(np % 3), (np / 3) & 1) &&
-              mbar_test_wait(bars.av(np % 3), (np / 3) & 1)) {
-            tc_fence_after();
-            mma_ts_x8<kL, 2 * kL, 3 * kL, 4 * kL, 5 * kL, 6 * kL, 7 * kL>(
-                tmem + C::kTO, tmem + C::kTAV + 64 * (np % 3), p_desc + (uint64_t)(((np % 3) * C::kPBytes) >> 4),
-                id_pv, np > 0 ? 1u : 0u);
-            tc_commit(bars.pv(np % 3));
-            ++np;
-            did = true;
-          }
-          if (!did) {
-            if (*abort_flag) break;
-            ++idle;
-            if ((idle & 63) == 0) {
-              const uint64_t t = now_ns();
-              if (idle_since == 0) {
-                idle_since = t;
-              } else if (t - idle_since > kSpinNs || idle > kIssuerPolls) {
-                *abort_flag = 1u;
-                atomicOr(&g_tq_device_error, 1u);
-                break;
-              }
+    } else if (C::kStreams == 2 || warp == 1) {
+      constexpr uint32_t kL = C::kLine;  // P' line bytes: 16 lines per K-step
+      constexpr uint32_t id_qk = idesc_f16(128, NR, 0, 0);
+      constexpr uint32_t id_pv = idesc_f16(128, NR, 0, 1);
+      constexpr uint32_t kQ1 = NR * 8;  // second 64-coordinate block of Q, in 16-byte units
+      const uint64_t q_desc = smem_desc(sbase + C::kQ, 16, 1024, 2);
+      const uint64_t p_desc = smem_desc(sbase + C::kP, 16, 8 * C::kLine, C::kSwzMode);
+      // S^T(c) = K_hat(c) Q^T into S^T buffer c % kSbuf
+      auto issue_qk = [&](int c) {
+        tc_fence_after();
+        mma_ts_x8<2, 4, 6, kQ1, kQ1 + 2, kQ1 + 4, kQ1 + 6>(tmem + C::kTS + NR * (c % C::kSbuf),
+                                                           tmem + C::kTAK + 64 * (c & 1), q_desc, id_qk, 0u);
+        tc_commit(bars.sready(c % C::kSbuf));
+      };
+      // O^T += V^T P'^T(c) into the O^T of the chunk's stream (a stream's first P.V overwrites it)
+      auto issue_pv = [&](int c) {
+        tc_fence_after();
+        mma_ts_x8<kL, 2 * kL, 3 * kL, 4 * kL, 5 * kL, 6 * kL, 7 * kL>(
+            tmem + C::kTO + NR * (c % C::kStreams), tmem + C::kTAV + 64 * (c % 3),
+            p_desc + (uint64_t)(((c % 3) * C::kPBytes) >> 4), id_pv, c >= C::kStreams ? 1u : 0u);
+        tc_commit(bars.pv(c % 3));
+        if (C::kStreams == 2) tc_commit(bars.pvs(c & 1));
+      };
+      if constexpr (C::kStreams == 1) {
+        // ================= MMA issuer (64 rows; warp 1, one thread), never
+        // blocked on one operand while the other kind of MMA could go:
+        // S^T(c) once softmax(c - 2) released its buffer and the keys of
+        // chunk c are in tensor memory; P.V(c) once softmax(c) wrote P'(c)
+        // and the values of chunk c are in tensor memory.  S^T(c) is issued
+        // only after P.V(c - 3): a commit tracks every earlier MMA of this
+        // thread, so the completion of S^T(c) then also means that P.V(c - 3)
+        // is done, which frees P' buffer c % 3 and value buffer c % 3 without
+        // a wait of their own.
+        if (lane == 0) {
+          int nq = 0, np = 0;
+          uint32_t idle = 0;
+          uint64_t idle_since = 0;  // time of the first idle poll since the last issue
+          while (np < nchunks) {
+            bool did = false;
+            if (nq < nchunks && nq - 3 < np &&
+                (nq < C::kSbuf || mbar_test_wait(bars.sfree(nq % C::kSbuf), ((nq - C::kSbuf) / C::kSbuf) & 1)) &&
+                mbar_test_wait(bars.ak(nq & 3), (nq >> 2) & 1)) {
+              issue_qk(nq);
+              ++nq;
+              did = true;
             }
-            // no sleep between polls: a sleep's granularity (hundreds of
-            // cycles) would delay every MMA by as much
-          } else {
-            idle = 0;
-            idle_since = 0;
+            if (np < nq && mbar_test_wait(bars.pfull(np % 3), (np / 3) & 1) &&
+                mbar_test_wait(bars.av(np % 3), (np / 3) & 1)) {
+              issue_pv(np);
+              ++np;
+              did = true;
+            }
+            if (!did) {
+              if (*abort_flag) break;
+              ++idle;
+              if ((idle & 63) == 0) {
+                const uint64_t t = now_ns();
+                if (idle_since == 0) {
+                  idle_since = t;
+                } else if (t - idle_since > kSpinNs || idle >= (1u << 28)) {
+                  *abort_flag = 1u;
+                  atomicOr(&g_tq_device_error, 1u);
+                  break;
+                }
+              }
+            } else {
+              idle = 0;
+              idle_since = 0;
+            }
           }
+          // drain before tensor memory is freed
+          if (nq > 0) wait_bar(bars.sready((nq - 1) % C::kSbuf), ((nq - 1) / C::kSbuf) & 1, abort_flag, false);
+          if (np > 0) wait_bar(bars.pv((np - 1) % 3), ((np - 1) / 3) & 1, abort_flag, false);
         }
-        // drain before tensor memory is freed
-        if (nq > 0) wait_bar(bars.sready((nq - 1) & 1), ((nq - 1) >> 1) & 1, abort_flag, false);
-        if (np > 0) wait_bar(bars.pv((np - 1) % 3), ((np - 1) / 3) & 1, abort_flag, false);
+      } else if (lane == 0) {
+        // ================= MMA issuers (two streams), one thread each, so
+        // that the two kinds of MMA are issued in parallel (a batch of eight
+        // costs some hundreds of cycles to issue): warp 1 issues S^T(c) once
+        // the softmax released S^T buffer c % kSbuf and the keys of chunk c
+        // are in tensor memory; warp 0 issues P.V(c) once softmax(c) wrote
+        // P'(c) and the values of chunk c are in tensor memory.  P' buffer
+        // and value buffer c % 3 are reused for chunk c + 3 only after pv(c),
+        // which the softmax and the value dequant wait for.
+        int n = 0;
+        if (warp == 1) {
+          for (int c = 0; c < nchunks; ++c) {
+            if (c >= C::kSbuf && !poll_bar(bars.sfree(c % C::kSbuf), ((c - C::kSbuf) / C::kSbuf) & 1, abort_flag))
+              break;
+            if (!poll_bar(bars.ak(c & 3), (c >> 2) & 1, abort_flag)) break;
+            issue_qk(c);
+            n = c + 1;
+          }
+          if (n > 0) wait_bar(bars.sready((n - 1) % C::kSbuf), ((n - 1) / C::kSbuf) & 1, abort_flag, false);
+        } else {
+          for (int c = 0; c < nchunks; ++c) {
+            if (!poll_bar(bars.pfull(c % 3), (c / 3) & 1, abort_flag) ||
+                !poll_bar(bars.av(c % 3), (c / 3) & 1, abort_flag))
+              break;
+            issue_pv(c);
+            n = c + 1;
+          }
+          if (n > 0) wait_bar(bars.pv((n - 1) % 3), ((n - 1) / 3) & 1, abort_flag, false);
+        }
       }
       __syncwarp();
     }
@@ -640,9 +718,11 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     auto dq_keys = [&](int c) -> bool {
       const int st = c % C::kStages;
       bool ok = wait_bar(bars.full(st), (c / C::kStages) & 1, abort_flag);
-      if (ok && c >= 2) ok = wait_bar(bars.sready(c & 1), ((c - 2) >> 1) & 1, abort_flag);  // A_K[c % 2] read by S^T(c - 2)
-      // parameters [c % 4] were read by softmax(c - 4), which released S^T(c - 4)
-      // before S^T(c - 2) was issued
+      if (ok && c >= 2)  // A_K[c % 2] read by S^T(c - 2)
+        ok = wait_bar(bars.sready((c - 2) % C::kSbuf), ((c - 2) / C::kSbuf) & 1, abort_flag);
+      // parameters [c % kColP] were read by softmax(c - kColP), which in its
+      // stream precedes softmax(c - 2 - kSbuf), whose release of its S^T
+      // buffer let S^T(c - 2) be issued
       __syncwarp();
       if (!ok) return false;
       const uint8_t* stage = sm + C::kRing + st * C::kStageBytes;
@@ -716,23 +796,25 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
             rmin = nmin <= 0 ? 0 : max(0, nmin * a.group - row_off);  // first visible row of the tile
           }
         }
-        colp[(c & 3) * 128 + i] = make_float4(cs, sv, zv, __int_as_float(rmin));
+        colp[(c % C::kColP) * 128 + i] = make_float4(cs, sv, zv, __int_as_float(rmin));
       }
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(bars.ak(c & 3));
-        mbar_arrive(bars.sready(c & 1));
+        mbar_arrive(bars.sready(c % C::kSbuf));
       }
       return true;
     };
     // values of chunk c; then its ring stage is free
     auto dq_values = [&](int c) -> bool {
       const int st = c % C::kStages;
-      // A_V[c % 3] was read by P.V(c - 3), done once sready(c) is (the keys of
-      // chunk c, already dequantised, are its only other condition)
-      const bool ok = c < 3 || wait_bar(bars.sready(c & 1), (c >> 1) & 1, abort_flag);
+      // A_V[c % 3] was read by P.V(c - 3): done once sready(c) is with one
+      // MMA issuer (its commits track every earlier MMA); its own barrier
+      // with two
+      const bool ok = c < 3 || (C::kStreams == 1 ? wait_bar(bars.sready(c % C::kSbuf), (c / C::kSbuf) & 1, abort_flag)
+                                                 : wait_bar(bars.pv(c % 3), ((c - 3) / 3) & 1, abort_flag));
       __syncwarp();
       if (!ok) return false;
       // value codes of coordinate i, all 128 tokens -> A_V[c % 3]: word x of
@@ -780,7 +862,11 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     const int i = sw * 32 + lane;
     const uint32_t lane_q = (uint32_t)(sw * 32) << 16;
     const uint32_t bar_id = 1 + j;
-    const int row0 = kRS * j;
+    // 64 rows: rows [32 j, 32 j + 32) of every chunk; two streams: every row
+    // of chunks j, j + 2, ...
+    constexpr int kStr = C::kStreams;
+    const int row0 = kStr == 2 ? 0 : kRS * j;
+    const int c0 = kStr == 2 ? j : 0;
     float* red = reinterpret_cast<float*>(sm + C::kRed + j * C::kRedWG);
     float* nms = red;                                      // -m per row
     float* als = red + 32;                                 // rescale factor per row
@@ -816,20 +902,21 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
     // stored), then in place d = s * score_scale - m
     uint32_t x[kRS];
     bool pre = false;  // x already holds (or is loading) S^T(c)
-    for (int c = 0; c < nchunks; ++c) {
+    for (int c = c0; c < nchunks; c += kStr) {
       bool ok = !aborted;
+      const bool first = c < kStr;  // this warpgroup's first chunk
       if (!pre) {
-        ok = ok && wait_bar(bars.sready(c & 1), (c >> 1) & 1, abort_flag);
+        ok = ok && wait_bar(bars.sready(c % C::kSbuf), (c / C::kSbuf) & 1, abort_flag);
         __syncwarp();
         tc_fence_after();
-        tmem_ld<kRS>(s_base + NR * (c & 1), x);
+        tmem_ld<kRS>(s_base + NR * (c % C::kSbuf), x);
       }
       tc_wait_ld();
-      // S^T(c) is in registers: its buffer goes back to the MMA issuer (for S^T(c + 2))
+      const float4 cp = colp[(c % C::kColP) * 128 + i];
+      // S^T(c) is in registers: its buffer goes back to the MMA issuer (for S^T(c + kSbuf))
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars.sfree(c & 1));
-      const float4 cp = colp[(c & 3) * 128 + i];
+      if (lane == 0) mbar_arrive(bars.sfree(c % C::kSbuf));
       const int rmin = __float_as_int(cp.w);
       const bool masked = __any_sync(kFull, rmin > row0);
       float2* d = reinterpret_cast<float2*>(x);
@@ -866,8 +953,8 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       // vote: each row's largest p is then exactly 1.
       uint32_t ph[kH];
       const uint32_t fr = *fresh;
-      bool exact = c == 0;
-      if (c > 0) {
+      bool exact = first;
+      if (!first) {
 #pragma unroll
         for (int k = 0; k < kH; ++k) ph[k] = ex2_h2(d[k].x, d[k].y);
         // exact path: some score above m + 8 (p could leave the fp16 range),
@@ -932,15 +1019,19 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
             change |= fminf(fminf(al4.x, al4.y), fminf(al4.z, al4.w)) < 1.0f;
           }
         }
-        if (change && c > 0) {  // uniform across the warpgroup
-          // O^T holds chunks < c: rescale it after P.V(c - 1) has landed and
-          // before P.V(c) is issued (which needs this warpgroup's pfull)
-          if (!wait_bar(bars.pv((c - 1) % 3), ((c - 1) / 3) & 1, abort_flag)) aborted = true;
+        if (change && !first) {  // uniform across the warpgroup
+          // O^T (of this stream) holds its chunks < c: rescale it after the
+          // previous one's P.V has landed and before P.V(c) is issued (which
+          // needs this warpgroup's pfull); per-stream barriers in two-stream
+          // mode, since the other stream may move pv[] on by two phases
+          const bool got = kStr == 1 ? wait_bar(bars.pv((c - 1) % 3), ((c - 1) / 3) & 1, abort_flag)
+                                     : wait_bar(bars.pvs(j), ((c - 2 - j) >> 1) & 1, abort_flag);
+          if (!got) aborted = true;
           __syncwarp();
           tc_fence_after();
 #pragma unroll 1
           for (int g = 0; g < kRS / 8; ++g) {
-            const uint32_t o_addr = tmem + lane_q + C::kTO + row0 + 8 * g;
+            const uint32_t o_addr = tmem + lane_q + C::kTO + NR * (kStr == 2 ? j : 0) + row0 + 8 * g;
             uint32_t o[8];
             tmem_ld8(o_addr, o);
             tc_wait_ld();
@@ -979,16 +1070,19 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       // start loading S^T(c + 1) if it is already there (never wait for it here:
       // this chunk's pfull would then depend on S^T(c + 1))
       pre = false;
-      if (c + 1 < nchunks) {
-        const int cn = c + 1;
-        const bool rdy = mbar_test_wait(bars.sready(cn & 1), (cn >> 1) & 1);
+      if (c + kStr < nchunks) {
+        const int cn = c + kStr;
+        const bool rdy = mbar_test_wait(bars.sready(cn % C::kSbuf), (cn / C::kSbuf) & 1);
         if (__all_sync(kFull, rdy)) {
           tc_fence_after();
-          tmem_ld<kRS>(s_base + NR * (cn & 1), x);
+          tmem_ld<kRS>(s_base + NR * (cn % C::kSbuf), x);
           pre = true;
         }
       }
-      // P'[c % 3] was read by P.V(c - 3), done since sready(c) is
+      // P'[c % 3] was read by P.V(c - 3): done since sready(c) is with one MMA
+      // issuer; its own barrier with two
+      if (C::kStreams == 2 && c >= 3 && !aborted && !wait_bar(bars.pv(c % 3), ((c - 3) / 3) & 1, abort_flag))
+        aborted = true;
       uint8_t* pbuf = sm + C::kP + (c % 3) * C::kPBytes;
 #pragma unroll
       for (int q = 0; q < kRS / 8; ++q)
@@ -1026,67 +1120,154 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       }
     }
     named_bar(bar_id, 128);
-    if (i < kRS) {
-      float lrow = 0.f, zrow = 0.f;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        lrow += wsum[w * 32 + i];
-        zrow += wsum[128 + w * 32 + i];
-      }
-      const float inv = lrow > 0.f ? 1.0f / lrow : 0.f;
-      rcs[i] = make_float2(inv * 16777216.0f, zrow * inv);  // O^T holds codes as fp16 subnormals (code * 2^-24)
-      const int row = row_off + row0 + i;  // row of the kv-head's R
-      if (row0 + i < Rt) {
-        const float lse = (aborted || *abort_flag) ? CUDART_NAN_F
-                                                   : (lrow > 0.f ? (-nms[i] + log2f(lrow)) * kLn2 : -CUDART_INF_F);
-        if constexpr (FUSED) {
-          a.part_lse[(((long)b * a.Hk + kvh) * a.S + split) * a.R + row] = lse;
-        } else {
-          const long orow = ((long)(row / a.group) * a.B + b) * a.Hq + kvh * a.group + row % a.group;
-          a.part_lse[orow * a.S + split] = lse;
+    if constexpr (kStr == 1) {
+      if (i < kRS) {
+        float lrow = 0.f, zrow = 0.f;
+  #pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          lrow += wsum[w * 32 + i];
+          zrow += wsum[128 + w * 32 + i];
         }
-      }
-    }
-    if (nchunks > 0) {
-      const int lc = nchunks - 1;
-      if (!aborted && !wait_bar(bars.pv(lc % 3), (lc / 3) & 1, abort_flag)) aborted = true;
-      __syncwarp();
-      tc_fence_after();
-    }
-    named_bar(bar_id, 128);  // row constants ready
-    aborted = aborted || (*abort_flag != 0u);
-    {
-      // thread i holds coordinate i of its rows: each row is 32 consecutive
-      // floats per warp, one 128-byte store
-      uint32_t o[kRS];
-      if (nchunks > 0) {
-        tmem_ld<kRS>(tmem + lane_q + C::kTO + row0, o);
-        tc_wait_ld();
-      } else {
-#pragma unroll
-        for (int k = 0; k < kRS; ++k) o[k] = 0u;
-      }
-      if constexpr (FUSED) {
-        // the scratch partials of the single-launch verify are laid out
-        // [B][Hk][S][R][128] so that a CTA's rows are contiguous
-        float* dst = a.part_o + ((((long)b * a.Hk + kvh) * a.S + split) * a.R + row_off + row0) * kD + i;
-#pragma unroll
-        for (int k = 0; k < kRS; ++k) {
-          const float2 rc = rcs[k];
-          if (row0 + k < Rt) dst[k * kD] = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rc.x, rc.y);
-        }
-      } else {
-        int n = (row_off + row0) / a.group, jq = (row_off + row0) % a.group;
-#pragma unroll
-        for (int k = 0; k < kRS; ++k) {
-          const float2 rc = rcs[k];
-          if (row0 + k < Rt) {
-            const long orow = ((long)n * a.B + b) * a.Hq + kvh * a.group + jq;
-            a.part_o[(orow * a.S + split) * kD + i] = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rc.x, rc.y);
+        const float inv = lrow > 0.f ? 1.0f / lrow : 0.f;
+        rcs[i] = make_float2(inv * 16777216.0f, zrow * inv);  // O^T holds codes as fp16 subnormals (code * 2^-24)
+        const int row = row_off + row0 + i;  // row of the kv-head's R
+        if (row0 + i < Rt) {
+          const float lse = (aborted || *abort_flag) ? CUDART_NAN_F
+                                                     : (lrow > 0.f ? (-nms[i] + log2f(lrow)) * kLn2 : -CUDART_INF_F);
+          if constexpr (FUSED) {
+            a.part_lse[(((long)b * a.Hk + kvh) * a.S + split) * a.R + row] = lse;
+          } else {
+            const long orow = ((long)(row / a.group) * a.B + b) * a.Hq + kvh * a.group + row % a.group;
+            a.part_lse[orow * a.S + split] = lse;
           }
-          if (++jq == a.group) {
-            jq = 0;
-            ++n;
+        }
+      }
+      if (nchunks > 0) {
+        const int lc = nchunks - 1;
+        if (!aborted && !wait_bar(bars.pv(lc % 3), (lc / 3) & 1, abort_flag)) aborted = true;
+        __syncwarp();
+        tc_fence_after();
+      }
+      named_bar(bar_id, 128);  // row constants ready
+      aborted = aborted || (*abort_flag != 0u);
+      {
+        // thread i holds coordinate i of its rows: each row is 32 consecutive
+        // floats per warp, one 128-byte store
+        uint32_t o[kRS];
+        if (nchunks > 0) {
+          tmem_ld<kRS>(tmem + lane_q + C::kTO + row0, o);
+          tc_wait_ld();
+        } else {
+  #pragma unroll
+          for (int k = 0; k < kRS; ++k) o[k] = 0u;
+        }
+        if constexpr (FUSED) {
+          // the scratch partials of the single-launch verify are laid out
+          // [B][Hk][S][R][128] so that a CTA's rows are contiguous
+          float* dst = a.part_o + ((((long)b * a.Hk + kvh) * a.S + split) * a.R + row_off + row0) * kD + i;
+  #pragma unroll
+          for (int k = 0; k < kRS; ++k) {
+            const float2 rc = rcs[k];
+            if (row0 + k < Rt) dst[k * kD] = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rc.x, rc.y);
+          }
+        } else {
+          int n = (row_off + row0) / a.group, jq = (row_off + row0) % a.group;
+  #pragma unroll
+          for (int k = 0; k < kRS; ++k) {
+            const float2 rc = rcs[k];
+            if (row0 + k < Rt) {
+              const long orow = ((long)n * a.B + b) * a.Hq + kvh * a.group + jq;
+              a.part_o[(orow * a.S + split) * kD + i] = aborted ? CUDART_NAN_F : fmaf(__uint_as_float(o[k]), rc.x, rc.y);
+            }
+            if (++jq == a.group) {
+              jq = 0;
+              ++n;
+            }
+          }
+        }
+      }
+    } else {
+      // ---- two streams: stream j publishes (m, l, zero term) of every row;
+      // after both streams' last P.V, warpgroup j writes rows
+      // [j NR/2, (j + 1) NR/2) as the log-sum-exp merge of the two streams:
+      //   out = sum_j a_j (2^24 O_j + z_j) / sum_j a_j l_j,  a_j = 2^(m_j - M)
+      constexpr int kHalf = NR / 2;
+      float4* stc_mine = reinterpret_cast<float4*>(red + 576);  // [32] (m, l, z, -)
+      const float4* stc0 = reinterpret_cast<const float4*>(sm + C::kRed) + 144;
+      const float4* stc1 = reinterpret_cast<const float4*>(sm + C::kRed + C::kRedWG) + 144;
+      float4* rc4 = reinterpret_cast<float4*>(red + 704);  // [kHalf] (c_0, c_1, zero term, -)
+      if (i < kRS) {
+        float lrow = 0.f, zrow = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          lrow += wsum[w * 32 + i];
+          zrow += wsum[128 + w * 32 + i];
+        }
+        stc_mine[i] = make_float4(-nms[i], lrow, zrow, 0.f);
+      }
+      // last chunk of this stream (none if nchunks <= j)
+      const int lc = nchunks - 1 >= j ? nchunks - 1 - ((nchunks - 1 - j) & 1) : -1;
+      if (lc >= 0) {
+        if (!aborted && !wait_bar(bars.pv(lc % 3), (lc / 3) & 1, abort_flag)) aborted = true;
+        __syncwarp();
+        tc_fence_after();
+      }
+      named_bar(13, 128 * C::kSW);  // both streams' constants and last P.V
+      aborted = aborted || (*abort_flag != 0u);
+      const int h0 = j * kHalf;
+      if (i < kHalf) {
+        const float4 s0 = stc0[h0 + i], s1 = stc1[h0 + i];
+        const bool u0 = s0.y > 0.f, u1 = s1.y > 0.f;  // streams that saw the row
+        const float M = u0 && u1 ? fmaxf(s0.x, s1.x) : (u0 ? s0.x : s1.x);
+        const float a0 = u0 ? ex2(s0.x - M) : 0.f, a1 = u1 ? ex2(s1.x - M) : 0.f;
+        const float lsum = a0 * s0.y + a1 * s1.y;
+        const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+        // O^T holds codes as fp16 subnormals (code * 2^-24)
+        rc4[i] = make_float4(a0 * inv * 16777216.0f, a1 * inv * 16777216.0f, (a0 * s0.z + a1 * s1.z) * inv, 0.f);
+        const int row = row_off + h0 + i;  // row of the kv-head's R
+        if (h0 + i < Rt) {
+          const float lse = aborted ? CUDART_NAN_F : (lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -CUDART_INF_F);
+          if constexpr (FUSED) {
+            a.part_lse[(((long)b * a.Hk + kvh) * a.S + split) * a.R + row] = lse;
+          } else {
+            const long orow = ((long)(row / a.group) * a.B + b) * a.Hq + kvh * a.group + row % a.group;
+            a.part_lse[orow * a.S + split] = lse;
+          }
+        }
+      }
+      named_bar(bar_id, 128);
+      {
+        // thread i holds coordinate i of rows h0 .. h0 + kHalf of both streams
+        uint32_t o0[kHalf], o1[kHalf];
+#pragma unroll
+        for (int k = 0; k < kHalf; ++k) o0[k] = o1[k] = 0u;
+        if (nchunks > 0) tmem_ld<kHalf>(tmem + lane_q + C::kTO + h0, o0);
+        if (nchunks > 1) tmem_ld<kHalf>(tmem + lane_q + C::kTO + NR + h0, o1);
+        tc_wait_ld();
+        auto outv = [&](int k) -> float {
+          const float4 rc = rc4[k];
+          // a stream without visible tokens has weight 0 (its O^T may be unset)
+          const float v0 = rc.x != 0.f ? __uint_as_float(o0[k]) * rc.x : 0.f;
+          const float v1 = rc.y != 0.f ? __uint_as_float(o1[k]) * rc.y : 0.f;
+          return aborted ? CUDART_NAN_F : v0 + v1 + rc.z;
+        };
+        if constexpr (FUSED) {
+          float* dst = a.part_o + ((((long)b * a.Hk + kvh) * a.S + split) * a.R + row_off + h0) * kD + i;
+#pragma unroll
+          for (int k = 0; k < kHalf; ++k)
+            if (h0 + k < Rt) dst[k * kD] = outv(k);
+        } else {
+          int n = (row_off + h0) / a.group, jq = (row_off + h0) % a.group;
+#pragma unroll
+          for (int k = 0; k < kHalf; ++k) {
+            if (h0 + k < Rt) {
+              const long orow = ((long)n * a.B + b) * a.Hq + kvh * a.group + jq;
+              a.part_o[(orow * a.S + split) * kD + i] = outv(k);
+            }
+            if (++jq == a.group) {
+              jq = 0;
+              ++n;
+            }
           }
         }
       }
