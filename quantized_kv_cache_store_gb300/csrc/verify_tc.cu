@@ -100,8 +100,10 @@ struct Cfg {
   static constexpr int kStreams = NR == 64 ? 1 : 2;
   static constexpr int kRS = NR == 64 ? 32 : NR;  // query rows per softmax thread
   static constexpr int kSbuf = 2 * kStreams;      // S^T buffers
-  // token-parameter slots (chunk c: c % kColP), at least kSbuf + 2 (a power of two)
-  static constexpr int kColP = kStreams == 2 ? 8 : 4;
+  // token-parameter slots (chunk c: c % kColP): a slot is rewritten kSbuf + 2
+  // chunks on when the softmax reads chunk c's parameters before it releases
+  // S^T(c) (two streams), kSbuf + 4 when it reads them after (64 rows)
+  static constexpr int kColP = kStreams == 2 ? 8 : kSbuf + 4;
   static constexpr int kThreads = 256 + 128 * kSW;
   // per-thread register budgets after setmaxnreg (control / dequant /
   // softmax); their sum must stay within what the launch granted (checked at
@@ -720,9 +722,9 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
       bool ok = wait_bar(bars.full(st), (c / C::kStages) & 1, abort_flag);
       if (ok && c >= 2)  // A_K[c % 2] read by S^T(c - 2)
         ok = wait_bar(bars.sready((c - 2) % C::kSbuf), ((c - 2) / C::kSbuf) & 1, abort_flag);
-      // parameters [c % kColP] were read by softmax(c - kColP), which in its
-      // stream precedes softmax(c - 2 - kSbuf), whose release of its S^T
-      // buffer let S^T(c - 2) be issued
+      // parameters [c % kColP] were read by softmax(c - kColP) before it
+      // released S^T(c - kColP) (two streams), or it ended before softmax(c - 2 -
+      // kSbuf) started (64 rows); either release let S^T(c - 2) be issued
       __syncwarp();
       if (!ok) return false;
       const uint8_t* stage = sm + C::kRing + st * C::kStageBytes;
@@ -912,11 +914,13 @@ __global__ void __launch_bounds__(Cfg<PRESET, NR>::kThreads, 1)
         tmem_ld<kRS>(s_base + NR * (c % C::kSbuf), x);
       }
       tc_wait_ld();
-      const float4 cp = colp[(c % C::kColP) * 128 + i];
+      float4 cp;  // chunk c's parameters for token i (the order is the faster one per mode)
+      if constexpr (kStr == 2) cp = colp[(c % C::kColP) * 128 + i];
       // S^T(c) is in registers: its buffer goes back to the MMA issuer (for S^T(c + kSbuf))
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.sfree(c % C::kSbuf));
+      if constexpr (kStr == 1) cp = colp[(c % C::kColP) * 128 + i];
       const int rmin = __float_as_int(cp.w);
       const bool masked = __any_sync(kFull, rmin > row0);
       float2* d = reinterpret_cast<float2*>(x);
