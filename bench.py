@@ -164,19 +164,32 @@ def measured_peaks():
         return 6800.0, "fallback 6.8 TB/s"
 
 
+def kernel_source_digest(path: str) -> str:
+    """First 16 hex digits of the SHA-256 of a CUDA source with its // comments
+    and blank lines removed (a comment edit leaves the kernel unchanged)."""
+    import re
+
+    lines = []
+    for ln in open(path, encoding="utf-8").read().split("\n"):
+        ln = re.sub(r"//.*$", "", ln).rstrip()
+        if ln.strip():
+            lines.append(ln)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def ncu_traffic(kernel_tag: str, workload: str):
     """Per-launch DRAM bytes of the stage-1 kernel from the committed ncu
     summary, if it was taken on the current kernel source (else None)."""
     src = os.path.join(ROOT, "quantized_kv_cache_store_gb300", "csrc", "verify_tc.cu")
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}_ncu.txt")
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        sha = kernel_source_digest(src)
         vals = {}
         for line in open(path):
             if "=" in line and not line.lstrip().startswith("#"):
                 k, v = line.split("=", 1)
                 vals[k.strip()] = v.strip()
-        if vals.get("kernel_source_sha256_16") != sha:
+        if vals.get("kernel_source_digest") != sha:
             return None
         return float(vals["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -307,13 +320,15 @@ def bench_workload(name, args, rank, world, pg, dev_props, steps=None):
 
 
 def single_launch(sv) -> bool:
-    """Whether tq_verify / tq_store_verify run as one cooperative launch:
-    up to 64 rows per kv-head, up to 32 splits, every CTA resident (one per SM)."""
+    """Whether tq_verify / tq_store_verify run as one cooperative launch: up
+    to 32 splits and every CTA (split x kv-head x sequence x row tile of 64
+    rows) resident at once, one per SM."""
     import torch
 
     wl = sv.wl
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    return wl.n_spec * wl.Hq // wl.Hk <= 64 and sv.S <= 32 and sv.S * wl.Hk * wl.B <= sms
+    rtiles = (wl.n_spec * wl.Hq // wl.Hk + 63) // 64
+    return sv.S <= 32 and sv.S * wl.Hk * wl.B * rtiles <= sms
 
 
 def per_kernel_durations(sv, stream, G, n_caches):

@@ -35,10 +35,13 @@
 // bounded by 2^8 and the stale maximum is used (any reference point gives the
 // same softmax).
 //
-// Warp roles: warps 0, 2, 3 = producers (block ids + copies), warp 1 = MMA
-// issuer and TMEM owner; warpgroup 1 dequantises chunk c (A_K[c % 2], A_V[c % 3]
-// and the per-token parameters) while softmax warpgroup j (rows [32 j,
-// 32 j + 32)) works on an earlier chunk.  Every wait on an mbarrier is
+// Warp roles with 64 rows: warps 0, 2, 3 = producers (block ids + copies),
+// warp 1 = MMA issuer and TMEM owner; warpgroup 1 dequantises chunk c (A_K[c %
+// 2], A_V[c % 3] and the per-token parameters) while softmax warpgroup j (rows
+// [32 j, 32 j + 32)) works on an earlier chunk.  With up to 32 rows: warps 2, 3
+// = producers, warp 1 issues the S^T MMAs (and owns TMEM), warp 0 the P.V
+// MMAs, and softmax warpgroup j takes every row of chunks j, j + 2, ... (two
+// streams merged by log-sum-exp at the end).  Every wait on an mbarrier is
 // bounded: on expiry the CTA sets an abort flag and the sticky device error
 // word, drains its in-flight copies and MMAs, frees its tensor memory and
 // writes NaN partials.

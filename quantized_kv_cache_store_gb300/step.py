@@ -62,7 +62,7 @@ class SpecVerify:
         return self.out
 
     def verify_call(self, i: int = 0, stream=None) -> torch.Tensor:
-        """Both stages through tq_verify (one launch for up to 64 rows per kv-head)."""
+        """Both stages through tq_verify (one launch when every CTA fits on the device at once)."""
         tqkv.tq_verify(self.caches[i], self.preset, self.q, self.block_table, self.seq_lens, self.S,
                        self.wl.causal, self.part_o, self.part_lse, self.tickets, self.out, stream)
         return self.out

@@ -205,7 +205,7 @@ def tq_verify_stage2(partial_o: torch.Tensor, partial_lse: torch.Tensor, out: to
 def tq_verify(cache: torch.Tensor, preset: int, q: torch.Tensor, block_table: torch.Tensor,
               seq_lens: torch.Tensor, num_kv_splits: int, causal: bool, partial_o: torch.Tensor,
               partial_lse: torch.Tensor, tickets: torch.Tensor, out: torch.Tensor, stream=None) -> None:
-    """Both stages in one call (one launch for up to 64 rows per kv-head).
+    """Both stages in one call (one launch when S <= 32 and every CTA fits on the device at once).
     tickets: int32 [B, Hk, 4], zero before the first call, zero again after each."""
     d = cache_desc(cache, preset)
     n_spec, B, Hq, D = q.shape
