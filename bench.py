@@ -37,7 +37,7 @@ METRIC = "µs per spec-verify call and achieved HBM GB/s vs peak (k8v4, k3v4_nc)
 # seed offsets: the five configurations in order, then the PoC shape with the
 # other key widths
 CONFIG_INDEX = {"tiny_k8v4": 0, "poc_k8v4": 1, "poc_k3v4_nc": 2, "decode_k3v4_nc": 3, "longctx_k3v4_nc": 4,
-                "poc_k4v4_nc": 5, "poc_k2v4_nc": 6}
+                "poc_k4v4_nc": 5, "poc_k2v4_nc": 6, "cont_k8v4": 7}
 
 
 def parse_args():

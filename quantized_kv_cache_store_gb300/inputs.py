@@ -77,6 +77,10 @@ WORKLOADS = {
                             num_kv_splits=8),
     "poc_k2v4_nc": Workload("poc_k2v4_nc", "k2v4_nc", n_spec=8, B=4, Hq=32, Hk=4, seq_len=8192,
                             num_kv_splits=8),
+    # a continuation chunk of 128 query tokens (1024 rows per kv-head: 16 row
+    # tiles of 64 over the same pages) on the PoC cache
+    "cont_k8v4": Workload("cont_k8v4", "k8v4", n_spec=128, B=1, Hq=32, Hk=4, seq_len=8192,
+                          num_kv_splits=8),
 }
 
 
